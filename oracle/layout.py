@@ -1,0 +1,98 @@
+"""Oracle: byte layout of one 128-token KV page and one index page.
+
+Test infrastructure only (see ``oracle/__init__``).
+
+The pages fix the sizes: 128-token blocks (blog, "Sparse attention still scans
+an index"), 128 index bytes per token and layer (same section), and NVFP4 K+V
+at 576 bytes per token and layer for 4 KV heads of dimension 128 (ai4snews
+article, second paragraph: 34,560 bytes/token over the model's layers).  The
+placement of bytes inside a page is this library's own format, restated here
+independently of the CUDA code from its written specification:
+
+KV page, 73,728 bytes = 4 heads x 18,432 bytes; head g starts at g * 18,432:
+    +0      K codes   [128 tokens][64 B]  byte i = code(2i) | code(2i+1) << 4
+    +8,192  K scales  [8 groups][128 tokens]   E4M3, group k = channels 16k..16k+15
+    +9,216  V codes   [128 tokens][64 B]
+    +17,408 V scales  [8 groups][128 tokens]
+Index page, 16,384 bytes = [128 tokens][128 B] E4M3 index keys, where the
+16-byte chunk c of token t's row (dims 16c..16c+15) is stored at chunk
+position c XOR (t mod 8).
+
+Parity: pinned by the byte-count invariants of the pages
+(tests/test_oracle_nvfp4.py) and by the hand-placed bytes of
+tests/golden/layout_bytes.txt.
+"""
+
+import numpy as np
+
+PAGE_TOKENS = 128
+KV_HEADS = 4
+HEAD_DIM = 128
+IDX_DIM = 128
+HEAD_BYTES = 18_432
+KV_PAGE_BYTES = KV_HEADS * HEAD_BYTES          # 73,728
+IDX_PAGE_BYTES = PAGE_TOKENS * IDX_DIM        # 16,384
+OFF_KC, OFF_KS, OFF_VC, OFF_VS = 0, 8_192, 9_216, 17_408
+
+
+def pack_codes(codes):
+    """Pack E2M1 codes (last axis even) two per byte, element 2i in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 15) | ((c[..., 1::2] & 15) << 4)
+
+
+def unpack_codes(packed):
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & 15
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def write_kv_slot(pool, page, t, k_codes, k_scales, v_codes, v_scales):
+    """Write one token's NVFP4 K/V (codes [4,128], scales [4,8]) into slot t of a page.
+
+    ``pool`` is a uint8 array [n_pages, 73,728].
+    """
+    for g in range(KV_HEADS):
+        base = g * HEAD_BYTES
+        for off_c, off_s, codes, scales in ((OFF_KC, OFF_KS, k_codes, k_scales),
+                                            (OFF_VC, OFF_VS, v_codes, v_scales)):
+            row = base + off_c + t * 64
+            pool[page, row:row + 64] = pack_codes(codes[g])
+            for k in range(8):
+                pool[page, base + off_s + k * PAGE_TOKENS + t] = scales[g][k]
+
+
+def write_index_slot(pool, page, t, key_bytes):
+    """Write one token's 128 E4M3 index-key bytes into slot t (chunk-swizzled)."""
+    key_bytes = np.asarray(key_bytes, dtype=np.uint8)
+    for c in range(8):
+        pos = c ^ (t % 8)
+        start = t * IDX_DIM + pos * 16
+        pool[page, start:start + 16] = key_bytes[c * 16:(c + 1) * 16]
+
+
+def read_kv_slot(pool, page, t):
+    """Inverse of write_kv_slot: (k_codes, k_scales, v_codes, v_scales) of one slot."""
+    out = []
+    for off_c, off_s in ((OFF_KC, OFF_KS), (OFF_VC, OFF_VS)):
+        codes = np.zeros((KV_HEADS, HEAD_DIM), dtype=np.uint8)
+        scales = np.zeros((KV_HEADS, 8), dtype=np.uint8)
+        for g in range(KV_HEADS):
+            base = g * HEAD_BYTES
+            row = base + off_c + t * 64
+            codes[g] = unpack_codes(pool[page, row:row + 64])
+            for k in range(8):
+                scales[g, k] = pool[page, base + off_s + k * PAGE_TOKENS + t]
+        out += [codes, scales]
+    return tuple(out)
+
+
+def read_index_slot(pool, page, t):
+    key = np.zeros(IDX_DIM, dtype=np.uint8)
+    for c in range(8):
+        pos = c ^ (t % 8)
+        start = t * IDX_DIM + pos * 16
+        key[c * 16:(c + 1) * 16] = pool[page, start:start + 16]
+    return key
