@@ -1,0 +1,349 @@
+"""Benchmark of the NVFP4 block-sparse attention decode step on GB300.
+
+One step = indexer scan + top-16/recent selection + split sparse attention +
+LSE merge (the decode path's four kernels) over one batch of resident query
+tokens.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl gb300|reference]
+
+--impl reference times the CPU oracle (the plain float64 restatement of the
+method; there is no other reference implementation) on a bounded sample of
+the same workload on this host's cores.
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(replicas only: the path has no exchange step); the time is the max over ranks.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_kv_block_gb300 import harness, ops, workloads  # noqa: E402
+
+ROOFLINE_NOMINAL_GBS = 8000.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_kv_block_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(config_name):
+    """DRAM bytes per indexer launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "indexer_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(config_name)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [l.split(",") for l in out.strip().splitlines() if l.strip()]
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if "Active" in v and "Not" not in v:
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(wl, sel, n_sel):
+    """Bytes the step must move: index pages scanned + KV pages selected by any
+    query token of a sequence (576 B per valid token) + queries, weights,
+    output and metadata.  Workspace traffic is not counted."""
+    idx = wl.index_bytes()
+    kv = 0
+    qsl = wl.q_start_loc
+    for b in range(wl.n_seqs):
+        blocks = set()
+        for j in range(qsl[b], qsl[b + 1]):
+            blocks.update(int(x) for x in sel[j, : n_sel[j]])
+        L = wl.seq_lens[b]
+        for blk in blocks:
+            kv += 576 * min(128, L - 128 * blk)
+    T = wl.n_q_total
+    small = T * (16 * 128 + 8 * 128 + 8 * 4 + 16 * 128 * 4) + wl.n_seqs * (wl.max_pages * 4 + 8) + 4
+    return idx, kv, idx + kv + small
+
+
+def run_gpu(args, rank, world, local_rank):
+    dev = f"cuda:{local_rank}"
+    torch.cuda.set_device(local_rank)
+    wl = workloads.config(args.config)
+    st = harness.build_state(wl, dev)
+    q, qi, w = wl.queries(dev)
+    T = wl.n_q_total
+    n_splits = args.splits or ops.choose_splits(T)
+    bufs = ops.DecodeBuffers(T, wl.max_pages, n_splits, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        return ops.decode_step(st.cache, q, qi, w, st.block_table, st.seq_lens, st.q_start_loc, bufs)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    sel = bufs.sel.cpu().numpy()
+    n_sel = bufs.n_sel.cpu().numpy()
+    idx_bytes, kv_bytes, alg_bytes = algorithmic_bytes(wl, sel, n_sel)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        ops.indexer_topk(st.cache, qi, w, st.block_table, st.seq_lens, st.q_start_loc, ws=bufs.ws,
+                         sel=bufs.sel, n_sel=bufs.n_sel)
+        ev[i][1].record(stream)
+        ops.sparse_attn_decode(st.cache, q, bufs.sel, bufs.n_sel, st.block_table, st.seq_lens,
+                               st.q_start_loc, n_splits, o_part=bufs.o_part, lse_part=bufs.lse_part)
+        ops.merge_splits(bufs.o_part, bufs.lse_part, out=bufs.out)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    idx_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ms = float(np.mean(step_ms))
+    t_idx = float(np.mean(idx_ms))
+
+    # end to end through the public API: pinned host inputs -> device, step, output -> host
+    h_q = q.cpu().pin_memory()
+    h_qi = qi.cpu().pin_memory()
+    h_w = w.cpu().pin_memory()
+    h_bt = st.block_table.cpu().pin_memory()
+    h_sl = st.seq_lens.cpu().pin_memory()
+    h_qsl = st.q_start_loc.cpu().pin_memory()
+    h_out = torch.empty((T, 16, 128), dtype=torch.float32).pin_memory()
+    d_q, d_qi, d_w = torch.empty_like(q), torch.empty_like(qi), torch.empty_like(w)
+    d_bt, d_sl, d_qsl = (torch.empty_like(st.block_table), torch.empty_like(st.seq_lens),
+                         torch.empty_like(st.q_start_loc))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qi, h_w, h_bt, h_sl, h_qsl))
+    d2h = h_out.numel() * 4
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for d, h in ((d_q, h_q), (d_qi, h_qi), (d_w, h_w), (d_bt, h_bt), (d_sl, h_sl), (d_qsl, h_qsl)):
+            d.copy_(h, non_blocking=True)
+        out = ops.decode_step(st.cache, d_q, d_qi, d_w, d_bt, d_sl, d_qsl, bufs)
+        h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e = float(np.mean(e2e_ms))
+
+    if world > 1:
+        t = torch.tensor([ms, t_idx, e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, t_idx, e2e = (float(x) for x in t.cpu())
+    return dict(wl=wl, T=T, ms=ms, t_idx=t_idx, e2e=e2e, h2d=h2d, d2h=d2h, n_splits=n_splits,
+                idx_bytes=idx_bytes, kv_bytes=kv_bytes, alg_bytes=alg_bytes, clocks=clk,
+                launches=4 * args.steps)
+
+
+def oracle_sample(wl, device, budget_s):
+    """Time the CPU oracle (indexer + selection + attention) on query tokens of
+    the first sequences, repeated until budget_s seconds of oracle work."""
+    import oracle
+    from oracle import formats, nvfp4
+
+    q, qi, w = (x.cpu().numpy() for x in wl.queries(device))
+    amax = [0.0, 0.0]
+    for tensor in (0, 1):
+        s = wl.channel_scales(tensor, device)
+        for b in range(wl.n_seqs):
+            for c in range(wl.n_chunks(b)):
+                amax[tensor] = max(amax[tensor], float(wl.kv_chunk(tensor, b, c, device, s).abs().max()))
+    s_enc_k = nvfp4.tensor_encode_scale(np.float32(amax[0]))
+    s_enc_v = nvfp4.tensor_encode_scale(np.float32(amax[1]))
+    scale = np.float32(1 / math.sqrt(128))
+    # untimed preparation: oracle quantisation of the sampled sequences
+    prep = []
+    qsl = wl.q_start_loc
+    for b in range(min(2, wl.n_seqs)):
+        L = wl.seq_lens[b]
+        idx = formats.encode_e4m3(wl.tokens(2, b, 0, L, device).cpu().numpy().astype(np.float64))
+        prep.append((b, idx, None))
+    pages = {}
+    done, t_work = 0, 0.0
+    while t_work < budget_s:
+        for b, idx, _ in prep:
+            for j in range(qsl[b], qsl[b + 1]):
+                pos = wl.seq_lens[b] - wl.n_q[b] + (j - qsl[b])
+                r = pos // 128
+                t0 = time.perf_counter()
+                scores = oracle.indexer.block_scores(qi[j], w[j], idx, r)
+                sel = oracle.indexer.select(scores, r)
+                t_idx = time.perf_counter() - t0
+                # the selected pages' FP8 operands are prepared outside the timed region
+                ks, vs = [], []
+                for blk in sel:
+                    lo, hi = blk * 128, min(blk * 128 + 128, pos + 1)
+                    if (b, lo, hi) not in pages:
+                        kc, kk = nvfp4.quantize(wl.tokens(0, b, lo, hi, device).cpu().numpy(), s_enc_k)
+                        vc, vv = nvfp4.quantize(wl.tokens(1, b, lo, hi, device).cpu().numpy(), s_enc_v)
+                        pages[(b, lo, hi)] = (nvfp4.fp8_operand(kc, kk), nvfp4.fp8_operand(vc, vv))
+                    ks.append(pages[(b, lo, hi)][0])
+                    vs.append(pages[(b, lo, hi)][1])
+                k8, v8 = np.concatenate(ks), np.concatenate(vs)
+                t0 = time.perf_counter()
+                oracle.attention.attend(q[j], k8, v8, scale, s_enc_k, s_enc_v)
+                t_work += t_idx + time.perf_counter() - t0
+                done += 1
+    cores = len(os.sched_getaffinity(0))
+    seqs = ", ".join(str(b) for b, _, _ in prep)
+    return done / t_work, cores, f"{done} query tokens of sequence(s) {seqs} (indexer over the full context + attention), {t_work:.1f} s of oracle work"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = workloads.config(args.config)
+    config = {"workload": wl.name, "description": wl.description, "n_seqs": wl.n_seqs,
+              "query_tokens": wl.n_q_total, "context": list(sorted(set(wl.seq_lens)))[:4],
+              "page_tokens": 128, "q_heads": 16, "kv_heads": 4, "head_dim": 128,
+              "idx_heads": 8, "topk": 16, "l2": "512 MiB buffer written between timed steps",
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        qps, cores, sample = oracle_sample(wl, dev, args.cpu_budget)
+        line = {"impl": "reference", "metric": "decode query tokens/s (NVFP4 sparse attention)",
+                "value": qps, "unit": "queries/s", "n_gpus": 0, "steps": args.steps,
+                "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": qps, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": qps, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    r = run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    T = r["T"]
+    qps = world * T / (r["ms"] * 1e-3)
+    step_gbs = r["alg_bytes"] / (r["ms"] * 1e-3) / 1e9
+    idx_gbs = r["idx_bytes"] / (r["t_idx"] * 1e-3) / 1e9
+    line = {
+        "metric": "decode query tokens/s (NVFP4 sparse attention)", "value": qps, "unit": "queries/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/e2m1 in, f32 accum",
+        "data": "synthetic", "config": config,
+        "hbm": {"algorithmic_bytes_per_step": r["alg_bytes"], "index_bytes": r["idx_bytes"],
+                "kv_bytes": r["kv_bytes"], "achieved_gbs": step_gbs,
+                "frac_of_8tbs": step_gbs / ROOFLINE_NOMINAL_GBS,
+                f"frac_of_{peak_kind}": step_gbs / peak},
+        "roofline": {"kernel": "indexer (scan + top-k launches of msa_indexer_topk)", "bound": "hbm",
+                     "achieved": idx_gbs, "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak,
+                     "peak_kind": peak_kind, "traffic": committed_traffic(wl.name),
+                     "algorithmic_bytes_per_launch": r["idx_bytes"], "ms_per_launch": r["t_idx"]},
+        "e2e": {"value": world * T / (r["e2e"] * 1e-3), "unit": "queries/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e"]},
+        "gpu_launches": r["launches"], "n_splits": r["n_splits"], "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline:
+        qps_cpu, cores, sample = oracle_sample(r["wl"], "cuda", args.cpu_budget)
+        line["cpu_baseline"] = {"value": qps_cpu, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+/*
+ * msa.h -- C ABI of the block-sparse attention decode path over an NVFP4 KV cache
+ * (library libmsa.so, built for sm_103a).
+ *
+ * What the path computes (sources: "vLLM Delivers Day-0 Support for
+ * MiniMax-M3.1-Flash", yuxiaoba.github.io, sections "Sparse attention still
+ * scans an index" and "Capacity savings must pay for conversion"; ai4snews
+ * article on MiniMax-M3.1-Flash in vLLM, second and third paragraphs;
+ * kongchang.com article, "NVFP4 KV Cache and MoE Weights"):
+ *   - the KV cache lives in 128-token blocks (pages), K and V stored as NVFP4:
+ *     E2M1 values with one E4M3 scale per 16 channels and an fp32 per-tensor
+ *     encode scale;
+ *   - a lightweight indexer scores every cached token from FP8 index keys
+ *     (128 bytes per token), score(t) = sum_h w_h * ReLU(q_h . k_idx(t)),
+ *     takes the max per block, keeps the top-16 blocks (ties to the lower block
+ *     index) and always the most recent block;
+ *   - exact GQA attention (16 query heads over 4 KV heads, head dim 128) runs
+ *     over the selected tokens only, FP8 E4M3 queries against K/V dequantised
+ *     from NVFP4 to FP8, with an fp32 online softmax split over the context and
+ *     merged by log-sum-exp.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are DEVICE pointers unless a parameter says "host".  The library
+ *     never allocates, frees or synchronises (msa_read_status excepted); all
+ *     work is enqueued on `stream` (a cudaStream_t; NULL = legacy stream).
+ *   - Return value: MSA_OK (0) when the work was enqueued, or a negative
+ *     MSA_ERR_* code when host-side validation failed (nothing is enqueued).
+ *   - Data errors that only the device can see (a physical page id outside the
+ *     pool, a sequence with more query tokens than cached tokens, ...) OR a
+ *     MSA_STATUS_* bit into the cache's device status word; the offending item
+ *     is skipped.  No kernel traps, asserts or waits without a bound.
+ *   - Supported shape: 128-token pages, 4 KV heads, head dim 128, index dim
+ *     128, 8 indexer heads, 16 query heads (GQA group 4).  Anything else is
+ *     MSA_ERR_UNSUPPORTED_SHAPE.
+ *
+ * Page formats (one physical page id p addresses both pools):
+ *   KV page p at kv_pool + p * 73,728 bytes = 4 heads x 18,432 bytes; head g
+ *   at offset g * 18,432:
+ *     +0       K codes  [128 tokens][64 B]: byte i = code(ch 2i) | code(ch 2i+1) << 4
+ *     +8,192   K scales [8 groups][128 tokens]: E4M3 scale of channels 16k..16k+15
+ *     +9,216   V codes  [128 tokens][64 B]
+ *     +17,408  V scales [8 groups][128 tokens]
+ *   (576 bytes per token and layer: the 34,560 bytes/token of the ai4snews
+ *   article over the model's layers.)
+ *   Index page p at idx_pool + p * 16,384 bytes = [128 tokens][128 B] E4M3
+ *   index keys; the 16-byte chunk c of token t's row (dims 16c..16c+15) is
+ *   stored at chunk position c XOR (t mod 8).
+ *
+ * Sequences and query tokens: sequence b has seq_lens[b] cached tokens (the
+ * new query tokens already inserted) and q_start_loc[b+1] - q_start_loc[b]
+ * query tokens; query token j of b sits at position
+ * pos_j = seq_lens[b] - n_q + j, sees keys at positions <= pos_j, and its
+ * recent block is r_j = pos_j / 128.  block_table[b * max_pages + i] is the
+ * physical page of logical block i of sequence b.
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* msa_stream_t; /* same type as cudaStream_t */
+
+/* Host-side return codes. */
+#define MSA_OK 0
+#define MSA_ERR_INVALID_ARG (-1)      /* null pointer, negative size, ... */
+#define MSA_ERR_UNSUPPORTED_SHAPE (-2)
+#define MSA_ERR_WORKSPACE_TOO_SMALL (-3)
+#define MSA_ERR_LAUNCH_FAILED (-4)    /* a kernel launch returned an error */
+
+/* Sticky device status bits (OR-ed into *msa_cache.status). */
+#define MSA_STATUS_BAD_SLOT 0x1       /* slot_mapping points outside the pool */
+#define MSA_STATUS_BAD_PAGE 0x2       /* block_table entry outside the pool */
+#define MSA_STATUS_BAD_SEQ 0x4        /* n_q < 0, n_q > seq_len or seq_len > max_pages*128 */
+#define MSA_STATUS_BAD_SELECTION 0x8  /* a selected block id outside 0..r_j */
+
+/* The KV cache and its metadata.  Caller-owned; the library only reads it. */
+typedef struct msa_cache {
+  void* kv_pool;        /* device, n_pages * 73,728 bytes (format above) */
+  void* idx_pool;       /* device, n_pages * 16,384 bytes (format above) */
+  int64_t n_pages;      /* physical pages in both pools */
+  int32_t page_tokens;  /* must be 128 */
+  int32_t n_kv_heads;   /* must be 4 */
+  int32_t head_dim;     /* must be 128 */
+  int32_t idx_dim;      /* must be 128 */
+  float s_enc_k;        /* host value: fp32 per-tensor encode scale of K, > 0 */
+  float s_enc_v;        /* host value: fp32 per-tensor encode scale of V, > 0 */
+  int32_t* status;      /* device int32, sticky MSA_STATUS_* bits; may be NULL */
+} msa_cache;
+
+/*
+ * Quantise new tokens to NVFP4 / FP8 and write them into their cache slots.
+ * (NVFP4 KV cache: ai4snews article, second and third paragraphs; index keys of
+ * 128 FP8 bytes per token: blog, "Sparse attention still scans an index".)
+ *
+ *   k, v         fp32 [n_tokens][4][128], row-major, contiguous.
+ *   idx_k        fp32 [n_tokens][128] index keys.
+ *   slot_mapping int64 [n_tokens]: page * 128 + offset; a negative entry skips
+ *                the token.  A page >= n_pages sets MSA_STATUS_BAD_SLOT.
+ * Per (token, head, 16-channel group) with s = s_enc_k (K) or s_enc_v (V):
+ *   a = max|x|, sb = E4M3_RNE_satfinite(fp32(fp32(a / 6) * s)),
+ *   code = E2M1 round-to-nearest-even (ties to the even code, saturating at 6)
+ *          of fp32(|x| * s) / sb evaluated exactly, sign on non-zero codes only,
+ *          all codes 0 when sb == 0.
+ * Index keys: E4M3_RNE_satfinite(x); a zero result is stored as 0x00.
+ * Slots written by one call must be distinct.
+ */
+int msa_quantize_kv_insert(const msa_cache* cache, const float* k, const float* v,
+                           const float* idx_k, const int64_t* slot_mapping,
+                           int32_t n_tokens, msa_stream_t stream);
+
+/*
+ * Indexer scan and top-k selection (blog, "Sparse attention still scans an
+ * index": 16 blocks plus the most recent one; "Parallelize index work across
+ * context": the split scan keeps the selection exact).
+ *
+ *   q_idx       E4M3 [n_q_total][n_idx_heads = 8][128] index queries.
+ *   w           fp32 [n_q_total][8] head weights (>= 0 for the ReLU reading).
+ *   block_table int32 [n_seqs][max_pages]; seq_lens int32 [n_seqs];
+ *   q_start_loc int32 [n_seqs + 1], non-decreasing, q_start_loc[0] = 0,
+ *               q_start_loc[n_seqs] = n_q_total.
+ *   topk        must be 16.
+ *   sel         int32 [n_q_total][topk + 1] out: min(topk, r_j) selected block
+ *               ids of blocks 0..r_j-1 (highest block score first wins, ties to
+ *               the lower id) in ascending order, then r_j; padded with -1.
+ *   n_sel       int32 [n_q_total] out: min(topk, r_j) + 1.
+ *   ws, ws_bytes scratch of at least msa_indexer_workspace_bytes(...) bytes.
+ *               After the stream reaches the end of this call it holds the fp32
+ *               block scores S[j][i] (row stride max_pages) for i < r_j;
+ *               other entries are unspecified.
+ * Block score S[j][i] = max over the 128 tokens t of block i of
+ *   sum_h w[j][h] * max(0, q_idx[j][h] . key(t)), computed with fp32 sums of
+ *   exact FP8 products.
+ * n_seqs <= 4096.
+ */
+int msa_indexer_topk(const msa_cache* cache, const uint8_t* q_idx, const float* w,
+                     int32_t n_idx_heads, const int32_t* block_table, int32_t max_pages,
+                     const int32_t* seq_lens, const int32_t* q_start_loc, int32_t n_seqs,
+                     int32_t n_q_total, int32_t topk, int32_t* sel, int32_t* n_sel,
+                     void* ws, size_t ws_bytes, msa_stream_t stream);
+
+/* Bytes of scratch msa_indexer_topk needs (a multiple of 256). */
+size_t msa_indexer_workspace_bytes(int32_t n_q_total, int32_t max_pages);
+
+/*
+ * Split-context sparse GQA attention over the selected blocks (blog, "Sparse
+ * attention still scans an index": exact attention over the selected blocks;
+ * ai4snews article, third paragraph: FP8 queries, NVFP4 K/V dequantised to FP8
+ * before the matmul).
+ *
+ *   q           E4M3 [n_q_total][n_q_heads = 16][128] queries.
+ *   sel, n_sel  as written by msa_indexer_topk (any ascending or unordered
+ *               list of distinct block ids <= r_j is accepted).
+ *   n_splits    1..64: the selected blocks of each query token are dealt
+ *               round-robin to n_splits partial attentions.
+ *   o_part      fp32 [n_q_total][n_splits][16][128] out: each split's
+ *               normalised output (zero for an empty split).
+ *   lse_part    fp32 [n_q_total][n_splits][16] out: natural-log sum of exp of
+ *               the split's logits (-inf for an empty split).
+ * Per element the FP8 operand is sign(code) | E4M3_RNE(|e2m1(code)| * sb);
+ * logits = (q . k8) * softmax_scale / s_enc_k; the value contraction is
+ * divided by s_enc_v.  Keys after pos_j are masked.
+ */
+int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q_heads,
+                           float softmax_scale, const int32_t* sel, const int32_t* n_sel,
+                           const int32_t* block_table, int32_t max_pages,
+                           const int32_t* seq_lens, const int32_t* q_start_loc,
+                           int32_t n_seqs, int32_t n_q_total, int32_t n_splits,
+                           float* o_part, float* lse_part, msa_stream_t stream);
+
+/*
+ * Log-sum-exp merge of the split partials:
+ *   out[j][h] = sum_s exp(lse[j][s][h] - L) * o_part[j][s][h],
+ *   L = log sum_s exp(lse[j][s][h]).
+ *   out fp32 [n_q_total][n_q_heads][128].  A row whose splits are all empty
+ *   is written as zeros.
+ */
+int msa_merge_splits(const float* o_part, const float* lse_part, int32_t n_q_total,
+                     int32_t n_q_heads, int32_t n_splits, float* out, msa_stream_t stream);
+
+/*
+ * Helpers for the per-tensor scale.  msa_absmax folds max|x[i]| over n fp32
+ * values into *amax (device float, caller-initialised to 0): call it on every
+ * chunk of a tensor, then msa_encode_scale(amax) returns the fp32 encode scale
+ * 448 / amax (1 for amax == 0).
+ */
+int msa_absmax(const float* x, int64_t n, float* amax, msa_stream_t stream);
+float msa_encode_scale(float amax);
+
+/*
+ * Diagnostic: the FP8 operands the attention kernel multiplies, for one page.
+ * k8, v8: uint8 [4 heads][128 tokens][128 channels] out, E4M3 bytes in
+ * logical channel order, produced by the same device dequantiser as
+ * msa_sparse_attn_decode.
+ */
+int msa_debug_fp8_page(const msa_cache* cache, int64_t page, uint8_t* k8, uint8_t* v8,
+                       msa_stream_t stream);
+
+/* Copies the device status word to *host_out (synchronous on the stream). */
+int msa_read_status(const msa_cache* cache, int32_t* host_out, msa_stream_t stream);
+
+/* Static description of a return code or status bit set. */
+const char* msa_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H */

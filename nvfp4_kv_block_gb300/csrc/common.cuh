@@ -1,0 +1,163 @@
+// Shared device helpers of the NVFP4 sparse-attention decode kernels (sm_103a).
+//
+// Page formats and shapes follow include/msa.h.  The FP8 (E4M3) and FP4
+// (E2M1) conversions use the hardware round-to-nearest-even converters through
+// CUDA's cuda_fp8.h intrinsics.
+#pragma once
+
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+constexpr int kPageTokens = 128;
+constexpr int kKvHeads = 4;
+constexpr int kHeadDim = 128;
+constexpr int kIdxDim = 128;
+constexpr int kIdxHeads = 8;
+constexpr int kQHeads = 16;
+constexpr int kGqa = kQHeads / kKvHeads;
+constexpr int kTopK = 16;
+constexpr int kSelStride = kTopK + 1;
+constexpr int kHeadBytes = 18432;
+constexpr int kKvPageBytes = kKvHeads * kHeadBytes;  // 73,728
+constexpr int kIdxPageBytes = kPageTokens * kIdxDim;  // 16,384
+constexpr int kOffKc = 0, kOffKs = 8192, kOffVc = 9216, kOffVs = 17408;
+constexpr int kMaxSeqs = 4096;
+constexpr int kMaxSplits = 64;
+
+__device__ __forceinline__ void set_status(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// ---- loads -----------------------------------------------------------------
+// Streaming loads of read-only cache data: not kept in L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 v;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+  uint32_t v;
+  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// ---- byte permute ----------------------------------------------------------
+// PTX prmt.b32 (default mode): output byte n is byte (c >> 4n) & 7 of {b:a};
+// if bit 3 of that selector nibble is set, the selected byte's sign bit is
+// replicated over the output byte instead.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// ---- E4M3 helpers -----------------------------------------------------------
+__device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
+  return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+// Two floats -> two E4M3 bytes, x in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float x, float y) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)(byte & 0xFF), __NV_E4M3);
+  return __half2float(__half(h));
+}
+// Canonical zero: an E4M3 byte of zero magnitude becomes 0x00.
+__device__ __forceinline__ uint32_t canon_zero(uint32_t byte) {
+  return (byte & 0x7F) ? byte : 0u;
+}
+
+// Order-preserving map of an fp32 value to uint32 (larger float -> larger int).
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---- NVFP4 -> FP8 dequantisation --------------------------------------------
+// Table entry for scale byte sb: 8 E4M3 bytes, entry m = E4M3_RNE(|e2m1(m)| * sb),
+// magnitudes m = 0..7 -> 0, 0.5, 1, 1.5, 2, 3, 4, 6.  The product has at most
+// five significant bits, so it is exact in fp32 and the conversion is the only
+// rounding.  A zero result is stored as 0x00.
+__device__ __forceinline__ void build_dequant_table(uint2* tab, int tid, int nthreads) {
+  const float mags[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  for (int sb = tid; sb < 256; sb += nthreads) {
+    const float s = e4m3_to_f32((uint32_t)sb);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      lo |= canon_zero(f32_to_e4m3(mags[m] * s)) << (8 * m);
+      hi |= canon_zero(f32_to_e4m3(mags[m + 4] * s)) << (8 * m);
+    }
+    tab[sb] = make_uint2(lo, hi);
+  }
+}
+
+// Eight E2M1 codes (nibble k = element k) -> eight FP8 operand bytes
+// (x: elements 0..3, y: elements 4..7), each sign(code) | table[|code|].
+__device__ __forceinline__ uint2 dequant8(uint32_t w, uint2 t) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t mag0 = prmt(t.x, t.y, m);
+  const uint32_t mag1 = prmt(t.x, t.y, m >> 16);
+  // selector nibble 8|sign: picks byte 0 (0x00) or byte 1 (0x80) of 0x8000 and
+  // replicates its sign bit -> 0x00 / 0xFF per output byte
+  const uint32_t ssel = ((w >> 3) & 0x11111111u) | 0x88888888u;
+  const uint32_t s0 = prmt(0x8000u, 0u, ssel);
+  const uint32_t s1 = prmt(0x8000u, 0u, ssel >> 16);
+  return make_uint2(mag0 | (s0 & 0x80808080u), mag1 | (s1 & 0x80808080u));
+}
+
+// ---- tensor cores: mma.sync m16n8k32, E4M3 x E4M3 -> fp32 --------------------
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---- sequence metadata --------------------------------------------------------
+struct SeqInfo {
+  int seq_len;
+  int n_q;
+  int q0;
+  bool ok;
+};
+
+// Sequence b's metadata; ok is false (and the sequence must be skipped) when
+// its query tokens fall outside [0, n_q_total), n_q < 0, n_q > seq_len or the
+// context exceeds the block table row.
+__device__ __forceinline__ SeqInfo load_seq(int b, const int* seq_lens, const int* q_start_loc,
+                                            int max_pages, int n_q_total) {
+  SeqInfo s;
+  s.seq_len = seq_lens[b];
+  s.q0 = q_start_loc[b];
+  s.n_q = q_start_loc[b + 1] - s.q0;
+  s.ok = s.n_q >= 0 && s.q0 >= 0 && s.q0 + s.n_q <= n_q_total && s.seq_len >= s.n_q &&
+         s.seq_len <= max_pages * kPageTokens;
+  return s;
+}
+
+// Largest b in [0, n_seqs) with q_start_loc[b] <= j (q_start_loc non-decreasing).
+__device__ __forceinline__ int find_seq(const int* q_start_loc, int n_seqs, int j) {
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (q_start_loc[mid] <= j) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace msa

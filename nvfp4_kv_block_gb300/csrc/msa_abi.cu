@@ -1,0 +1,163 @@
+// C ABI of libmsa.so: host-side validation and kernel launches.  See
+// include/msa.h for the contract of every entry point.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace msa {
+cudaError_t launch_quantize_insert(const msa_cache*, const float*, const float*, const float*,
+                                   const int64_t*, int, cudaStream_t);
+cudaError_t launch_absmax(const float*, int64_t, float*, cudaStream_t);
+cudaError_t launch_indexer_topk(const msa_cache*, const uint8_t*, const float*, const int*, int,
+                                const int*, const int*, int, int, int*, int*, float*,
+                                cudaStream_t);
+cudaError_t launch_sparse_attn(const msa_cache*, const uint8_t*, float, const int*, const int*,
+                               const int*, int, const int*, const int*, int, int, int, float*,
+                               float*, cudaStream_t);
+cudaError_t launch_merge(const float*, const float*, int, int, int, float*, cudaStream_t);
+cudaError_t launch_debug_fp8_page(const msa_cache*, int64_t, uint8_t*, uint8_t*, cudaStream_t);
+}  // namespace msa
+
+namespace {
+
+constexpr int32_t kMaxPagesPerSeq = 65536;
+
+int check_cache(const msa_cache* c) {
+  if (!c || !c->kv_pool || !c->idx_pool || c->n_pages <= 0) return MSA_ERR_INVALID_ARG;
+  if (c->page_tokens != msa::kPageTokens || c->n_kv_heads != msa::kKvHeads ||
+      c->head_dim != msa::kHeadDim || c->idx_dim != msa::kIdxDim)
+    return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (!(c->s_enc_k > 0.f) || !(c->s_enc_v > 0.f) || !isfinite(c->s_enc_k) || !isfinite(c->s_enc_v))
+    return MSA_ERR_INVALID_ARG;
+  return MSA_OK;
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_LAUNCH_FAILED; }
+
+}  // namespace
+
+extern "C" {
+
+int msa_quantize_kv_insert(const msa_cache* cache, const float* k, const float* v,
+                           const float* idx_k, const int64_t* slot_mapping, int32_t n_tokens,
+                           msa_stream_t stream) {
+  if (int rc = check_cache(cache)) return rc;
+  if (n_tokens < 0) return MSA_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!k || !v || !idx_k || !slot_mapping)) return MSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(idx_k)) & 15)
+    return MSA_ERR_INVALID_ARG;  // float4 loads
+  return launched(msa::launch_quantize_insert(cache, k, v, idx_k, slot_mapping, n_tokens,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t msa_indexer_workspace_bytes(int32_t n_q_total, int32_t max_pages) {
+  if (n_q_total <= 0 || max_pages <= 0) return 256;
+  const size_t b = (size_t)n_q_total * (size_t)max_pages * sizeof(float);
+  return (b + 255) / 256 * 256;
+}
+
+int msa_indexer_topk(const msa_cache* cache, const uint8_t* q_idx, const float* w,
+                     int32_t n_idx_heads, const int32_t* block_table, int32_t max_pages,
+                     const int32_t* seq_lens, const int32_t* q_start_loc, int32_t n_seqs,
+                     int32_t n_q_total, int32_t topk, int32_t* sel, int32_t* n_sel, void* ws,
+                     size_t ws_bytes, msa_stream_t stream) {
+  if (int rc = check_cache(cache)) return rc;
+  if (n_idx_heads != msa::kIdxHeads || topk != msa::kTopK) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_seqs < 0 || n_q_total < 0 || max_pages <= 0) return MSA_ERR_INVALID_ARG;
+  if (n_seqs > msa::kMaxSeqs || max_pages > kMaxPagesPerSeq) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_q_total > 0 && (!q_idx || !w || !block_table || !seq_lens || !q_start_loc || !sel ||
+                        !n_sel || !ws || n_seqs == 0))
+    return MSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_idx) & 15) || (reinterpret_cast<uintptr_t>(w) & 7) ||
+      (reinterpret_cast<uintptr_t>(ws) & 15))
+    return MSA_ERR_INVALID_ARG;
+  if (ws_bytes < msa_indexer_workspace_bytes(n_q_total, max_pages))
+    return MSA_ERR_WORKSPACE_TOO_SMALL;
+  return launched(msa::launch_indexer_topk(cache, q_idx, w, block_table, max_pages, seq_lens,
+                                           q_start_loc, n_seqs, n_q_total, sel, n_sel,
+                                           static_cast<float*>(ws),
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q_heads,
+                           float softmax_scale, const int32_t* sel, const int32_t* n_sel,
+                           const int32_t* block_table, int32_t max_pages,
+                           const int32_t* seq_lens, const int32_t* q_start_loc, int32_t n_seqs,
+                           int32_t n_q_total, int32_t n_splits, float* o_part, float* lse_part,
+                           msa_stream_t stream) {
+  if (int rc = check_cache(cache)) return rc;
+  if (n_q_heads != msa::kQHeads) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_splits < 1 || n_splits > msa::kMaxSplits || n_q_total < 0 || n_seqs < 0 ||
+      max_pages <= 0 || !(softmax_scale > 0.f) || !isfinite(softmax_scale))
+    return MSA_ERR_INVALID_ARG;
+  if (n_q_total > 65535) return MSA_ERR_UNSUPPORTED_SHAPE;  // grid.z
+  if (n_q_total > 0 && (!q || !sel || !n_sel || !block_table || !seq_lens || !q_start_loc ||
+                        !o_part || !lse_part || n_seqs == 0))
+    return MSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q) & 15) return MSA_ERR_INVALID_ARG;
+  return launched(msa::launch_sparse_attn(cache, q, softmax_scale, sel, n_sel, block_table,
+                                          max_pages, seq_lens, q_start_loc, n_seqs, n_q_total,
+                                          n_splits, o_part, lse_part,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_merge_splits(const float* o_part, const float* lse_part, int32_t n_q_total,
+                     int32_t n_q_heads, int32_t n_splits, float* out, msa_stream_t stream) {
+  if (n_q_total < 0 || n_q_heads <= 0 || n_splits < 1 || n_splits > msa::kMaxSplits)
+    return MSA_ERR_INVALID_ARG;
+  if (n_q_total > 0 && (!o_part || !lse_part || !out)) return MSA_ERR_INVALID_ARG;
+  return launched(msa::launch_merge(o_part, lse_part, n_q_total, n_q_heads, n_splits, out,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_absmax(const float* x, int64_t n, float* amax, msa_stream_t stream) {
+  if (n < 0 || !amax || (n > 0 && !x)) return MSA_ERR_INVALID_ARG;
+  return launched(msa::launch_absmax(x, n, amax, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+float msa_encode_scale(float amax) {
+  if (!(amax > 0.f) || !isfinite(amax)) return 1.0f;
+  volatile float num = 448.0f;  // one IEEE fp32 division, as the quantiser reading states
+  return num / amax;
+}
+
+int msa_debug_fp8_page(const msa_cache* cache, int64_t page, uint8_t* k8, uint8_t* v8,
+                       msa_stream_t stream) {
+  if (int rc = check_cache(cache)) return rc;
+  if (page < 0 || page >= cache->n_pages || !k8 || !v8) return MSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k8) | reinterpret_cast<uintptr_t>(v8)) & 15)
+    return MSA_ERR_INVALID_ARG;
+  return launched(
+      msa::launch_debug_fp8_page(cache, page, k8, v8, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_read_status(const msa_cache* cache, int32_t* host_out, msa_stream_t stream) {
+  if (!cache || !host_out) return MSA_ERR_INVALID_ARG;
+  if (!cache->status) {
+    *host_out = 0;
+    return MSA_OK;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_out, cache->status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return MSA_ERR_LAUNCH_FAILED;
+  return cudaStreamSynchronize(s) == cudaSuccess ? MSA_OK : MSA_ERR_LAUNCH_FAILED;
+}
+
+const char* msa_status_string(int code) {
+  switch (code) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MSA_ERR_LAUNCH_FAILED: return "kernel launch failed";
+    case MSA_STATUS_BAD_SLOT: return "device: slot outside the pool";
+    case MSA_STATUS_BAD_PAGE: return "device: block table entry outside the pool";
+    case MSA_STATUS_BAD_SEQ: return "device: inconsistent sequence lengths / query counts";
+    case MSA_STATUS_BAD_SELECTION: return "device: selected block outside 0..r_j";
+    default: return code > 0 ? "device: several status bits" : "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,244 @@
+"""GPU parity: every kernel of libmsa.so against the CPU oracle, through the C ABI.
+
+Rules (the decode path's acceptance rules):
+  * quantised bytes and scales bit-exact;
+  * selected block sets exact, except swaps whose oracle block scores differ
+    from the selection cut-off by < 1e-4 relative;
+  * attention output max-abs error <= 2e-3 * max|V^| (fp32 accumulation), with
+    max|V^| the largest dequantised |V| among the pages the oracle attends.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import formats, layout, nvfp4
+from nvfp4_kv_block_gb300 import harness, ops, workloads
+
+from _parity import OracleSide, selection_ok, softmax_scale
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+ATOL_REL = 2e-3
+
+
+def _small_workload():
+    # short (r <= 16), exact page multiples, a boundary-straddling speculative
+    # batch, an empty sequence, a longer one with top-16 active; pages permuted
+    return workloads.custom("small_mixed", [1, 127, 0, 128, 129, 2053, 4096, 130, 5000],
+                            [1, 1, 0, 2, 8, 8, 3, 8, 5], seed=77, permuted=True)
+
+
+@pytest.fixture(scope="module")
+def small():
+    wl = _small_workload()
+    st = harness.build_state(wl, DEV)
+    return wl, st, OracleSide(wl, DEV)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    wl = workloads.config(0)
+    st = harness.build_state(wl, DEV)
+    return wl, st, OracleSide(wl, DEV)
+
+
+def _decode(wl, st, n_splits=None):
+    q, qi, w = wl.queries(DEV)
+    T = wl.n_q_total
+    n_splits = n_splits or ops.choose_splits(T)
+    bufs = ops.DecodeBuffers(T, wl.max_pages, n_splits, DEV)
+    out = ops.decode_step(st.cache, q, qi, w, st.block_table, st.seq_lens, st.q_start_loc, bufs)
+    torch.cuda.synchronize()
+    S = ops.block_scores_view(bufs.ws, T, wl.max_pages).cpu().numpy()
+    return bufs, out.cpu().numpy(), S
+
+
+def _check_tokens(wl, side, bufs, out, S, tokens):
+    sel = bufs.sel.cpu().numpy()
+    n_sel = bufs.n_sel.cpu().numpy()
+    worst = 0.0
+    for j in tokens:
+        b, pos, osel, oscores = side.token(j)
+        r = pos // 128
+        gsel = [int(x) for x in sel[j, : n_sel[j]]]
+        # block scores: fp32 sums of exact FP8 products vs exact float64
+        if r > 0:
+            ref = np.asarray(oscores)
+            err = np.max(np.abs(S[j, :r] - ref)) / max(1e-30, np.max(np.abs(ref)))
+            assert err < 1e-4, (j, err)
+        ok, diff = selection_ok(gsel, osel, oscores)
+        assert ok, (j, gsel, osel, diff)
+        assert sorted(gsel) == gsel and gsel[-1] == r and len(gsel) == min(16, r) + 1
+        assert all(v == -1 for v in sel[j, n_sel[j]:])
+        ref_out, _, vmax = side.attend(j, gsel if gsel == osel else osel, softmax_scale())
+        if gsel != osel:
+            continue  # allowed swap: the output is checked against the same selection below
+        e = np.max(np.abs(out[j] - ref_out))
+        worst = max(worst, e / vmax)
+        assert e <= ATOL_REL * vmax, (j, e, vmax)
+    return worst
+
+
+def test_encode_scale_and_absmax_match_oracle():
+    g = torch.Generator(device=DEV).manual_seed(5)
+    x = torch.randn(1_000_003, generator=g, device=DEV) * 3.7
+    amax = torch.zeros(1, dtype=torch.float32, device=DEV)
+    ops.absmax_(x[:500_000], amax)
+    ops.absmax_(x[500_000:], amax)
+    ref = float(x.abs().max())
+    assert float(amax) == ref
+    for a in [ref, 1.0, 448.0, 1e-3, 123.456]:
+        assert ops.encode_scale(a) == float(nvfp4.tensor_encode_scale(np.float32(a)))
+
+
+def test_insert_is_bit_exact(small):
+    wl, st, side = small
+    kv = st.cache.kv_pool.cpu().numpy()
+    ip = st.cache.idx_pool.cpu().numpy()
+    bt = wl.block_table()
+    assert side.s_enc_k == np.float32(st.cache.s_enc_k) and side.s_enc_v == np.float32(st.cache.s_enc_v)
+    for b in range(wl.n_seqs):
+        for blk in range(wl.pages_per_seq[b]):
+            want_kv, want_idx = side.page_bytes(b, blk)
+            phys = bt[b, blk]
+            assert np.array_equal(kv[phys], want_kv), (b, blk)
+            assert np.array_equal(ip[phys], want_idx), (b, blk)
+    assert st.cache.read_status() == 0
+
+
+def test_fp8_dequant_matches_oracle_for_every_scale_byte():
+    rng = np.random.default_rng(11)
+    pool = np.zeros((2, layout.KV_PAGE_BYTES), dtype=np.uint8)
+    kc = rng.integers(0, 16, (128, 4, 128)).astype(np.uint8)
+    vc = rng.integers(0, 16, (128, 4, 128)).astype(np.uint8)
+    # every one of the 256 scale bytes appears in K and in V
+    ks = rng.permutation(np.resize(np.arange(256), 128 * 4 * 8)).reshape(128, 4, 8).astype(np.uint8)
+    vs = rng.permutation(np.resize(np.arange(256), 128 * 4 * 8)).reshape(128, 4, 8).astype(np.uint8)
+    for t in range(128):
+        layout.write_kv_slot(pool, 1, t, kc[t], ks[t], vc[t], vs[t])
+    cache = ops.KVCache(2, 1.0, 1.0, DEV)
+    cache.kv_pool.copy_(torch.from_numpy(pool))
+    k8, v8 = ops.debug_fp8_page(cache, 1)
+    k8 = k8.cpu().numpy().transpose(1, 0, 2)  # -> [token, head, ch]
+    v8 = v8.cpu().numpy().transpose(1, 0, 2)
+    assert np.array_equal(k8, nvfp4.fp8_operand(kc, ks))
+    assert np.array_equal(v8, nvfp4.fp8_operand(vc, vs))
+
+
+def test_fp8_dequant_of_inserted_pages(tiny):
+    wl, st, side = tiny
+    bt = wl.block_table()
+    for blk in (0, 13, 31):
+        k8, v8 = ops.debug_fp8_page(st.cache, int(bt[0, blk]))
+        d = side.kv_tokens(0, blk * 128, blk * 128 + 128)
+        assert np.array_equal(k8.cpu().numpy().transpose(1, 0, 2), d["k8"])
+        assert np.array_equal(v8.cpu().numpy().transpose(1, 0, 2), d["v8"])
+
+
+def test_tiny_decode_matches_oracle(tiny):
+    wl, st, side = tiny
+    bufs, out, S = _decode(wl, st)
+    _check_tokens(wl, side, bufs, out, S, range(wl.n_q_total))
+    assert st.cache.read_status() == 0
+
+
+def test_small_mixed_decode_matches_oracle(small):
+    wl, st, side = small
+    bufs, out, S = _decode(wl, st)
+    _check_tokens(wl, side, bufs, out, S, range(wl.n_q_total))
+    assert st.cache.read_status() == 0
+
+
+@pytest.mark.parametrize("n_splits", [1, 2, 5, 17, 64])
+def test_attention_with_oracle_selection_any_split_count(small, n_splits):
+    wl, st, side = small
+    q, _, _ = wl.queries(DEV)
+    T = wl.n_q_total
+    sel = np.full((T, 17), -1, dtype=np.int32)
+    n_sel = np.zeros(T, dtype=np.int32)
+    refs = []
+    for j in range(T):
+        _, _, osel, _ = side.token(j)
+        sel[j, : len(osel)] = osel
+        n_sel[j] = len(osel)
+        refs.append(side.attend(j, osel, softmax_scale()))
+    o_part, lse = ops.sparse_attn_decode(st.cache, q, torch.from_numpy(sel).to(DEV),
+                                         torch.from_numpy(n_sel).to(DEV), st.block_table, st.seq_lens,
+                                         st.q_start_loc, n_splits)
+    out = ops.merge_splits(o_part, lse).cpu().numpy()
+    for j, (ref, ref_lse, vmax) in enumerate(refs):
+        assert np.max(np.abs(out[j] - ref)) <= ATOL_REL * vmax
+    if n_splits == 1:  # a single split carries the full log-sum-exp
+        for j, (_, ref_lse, _) in enumerate(refs):
+            assert np.allclose(lse[j, 0].cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_full_size_config_sampled(cfg):
+    wl = workloads.config(cfg)
+    st = harness.build_state(wl, DEV)
+    side = OracleSide(wl, DEV)
+    bufs, out, S = _decode(wl, st)
+    T = wl.n_q_total
+    rng = np.random.default_rng(1000 + cfg)
+    tokens = sorted(set([0, T // 2, T - 1] + [int(x) for x in rng.integers(0, T, 2)]))
+    _check_tokens(wl, side, bufs, out, S, tokens)
+    # sampled pages bit-exact, including the partial last page of a sequence
+    kv = st.cache.kv_pool
+    ip = st.cache.idx_pool
+    bt = wl.block_table()
+    for _ in range(3):
+        b = int(rng.integers(0, wl.n_seqs))
+        blk = int(rng.integers(0, wl.pages_per_seq[b]))
+        for blk_ in (blk, wl.pages_per_seq[b] - 1):
+            want_kv, want_idx = side.page_bytes(b, blk_)
+            phys = int(bt[b, blk_])
+            assert np.array_equal(kv[phys].cpu().numpy(), want_kv)
+            assert np.array_equal(ip[phys].cpu().numpy(), want_idx)
+    assert st.cache.read_status() == 0
+
+
+def test_host_validation_errors(tiny):
+    wl, st, _ = tiny
+    q, qi, w = wl.queries(DEV)
+    T = wl.n_q_total
+    with pytest.raises(ops.MsaError, match="workspace too small"):
+        ops.indexer_topk(st.cache, qi, w, st.block_table, st.seq_lens, st.q_start_loc,
+                         ws=torch.empty(16, dtype=torch.uint8, device=DEV))
+    with pytest.raises(ops.MsaError, match="invalid argument"):
+        ops.sparse_attn_decode(st.cache, q, torch.zeros((T, 17), dtype=torch.int32, device=DEV),
+                               torch.zeros(T, dtype=torch.int32, device=DEV), st.block_table,
+                               st.seq_lens, st.q_start_loc, n_splits=0)
+    bad = ops.KVCache(1, 1.0, 1.0, DEV)
+    bad.s_enc_k = float("nan")
+    with pytest.raises(ops.MsaError, match="invalid argument"):
+        ops.quantize_kv_insert(bad, torch.zeros((1, 4, 128), device=DEV), torch.zeros((1, 4, 128), device=DEV),
+                               torch.zeros((1, 128), device=DEV), torch.zeros(1, dtype=torch.int64, device=DEV))
+
+
+def test_device_status_bits_without_faults(tiny):
+    wl, st, _ = tiny
+    q, qi, w = wl.queries(DEV)
+    # a block table entry outside the pool: flagged, skipped, no fault
+    bt = st.block_table.clone()
+    bt[0, 3] = wl.total_pages + 5
+    cache = ops.KVCache(st.cache.n_pages, st.cache.s_enc_k, st.cache.s_enc_v, DEV)
+    cache.kv_pool, cache.idx_pool = st.cache.kv_pool, st.cache.idx_pool
+    bufs = ops.DecodeBuffers(wl.n_q_total, wl.max_pages, 2, DEV)
+    ops.decode_step(cache, q, qi, w, bt, st.seq_lens, st.q_start_loc, bufs)
+    assert cache.read_status() & 0x2
+    # a slot outside the pool
+    cache2 = ops.KVCache(1, 1.0, 1.0, DEV)
+    ops.quantize_kv_insert(cache2, torch.ones((2, 4, 128), device=DEV), torch.ones((2, 4, 128), device=DEV),
+                           torch.ones((2, 128), device=DEV),
+                           torch.tensor([5, 128 * 7], dtype=torch.int64, device=DEV))
+    assert cache2.read_status() & 0x1
+    # more query tokens than cached tokens
+    cache3 = ops.KVCache(st.cache.n_pages, st.cache.s_enc_k, st.cache.s_enc_v, DEV)
+    cache3.kv_pool, cache3.idx_pool = st.cache.kv_pool, st.cache.idx_pool
+    sl = torch.tensor([0], dtype=torch.int32, device=DEV)
+    ops.decode_step(cache3, q, qi, w, st.block_table, sl, st.q_start_loc, bufs)
+    assert cache3.read_status() & 0x4
