@@ -145,37 +145,73 @@ def run_gpu(args, rank, world, local_rank):
     def step():
         return ops.decode_step(st.cache, q, qi, w, st.block_table, st.seq_lens, st.q_start_loc, bufs)
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step()
+    step()
     torch.cuda.synchronize()
     sel = bufs.sel.cpu().numpy()
     n_sel = bufs.n_sel.cpu().numpy()
     idx_bytes, kv_bytes, alg_bytes = algorithmic_bytes(wl, sel, n_sel)
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # the step as one CUDA graph (scan, top-k, attention, merge: chained with
+    # programmatic dependent launch) so that host launch latency does not gap
+    # the kernels; a second graph holds the indexer alone for its own timing
+    def run_indexer():
+        ops.indexer_topk(st.cache, qi, w, st.block_table, st.seq_lens, st.q_start_loc, ws=bufs.ws,
+                         sel=bufs.sel, n_sel=bufs.n_sel)
+
+    def run_attention():
+        ops.sparse_attn_decode(st.cache, q, bufs.sel, bufs.n_sel, st.block_table, st.seq_lens,
+                               st.q_start_loc, n_splits, o_part=bufs.o_part, lse_part=bufs.lse_part)
+        ops.merge_splits(bufs.o_part, bufs.lse_part, out=bufs.out)
+
+    def run_step():
+        run_indexer()
+        run_attention()
+
+    if args.eager:
+        g_step, g_idx = run_step, run_indexer
+    else:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            run_step()
+        stream.wait_stream(side)
+        graph_s, graph_i = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_s):
+            run_step()
+        with torch.cuda.graph(graph_i):
+            run_indexer()
+        g_step, g_idx = graph_s.replay, graph_i.replay
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        g_step()
+        flush.fill_(1.0)
+        g_idx()
+    torch.cuda.synchronize()
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
     clocks = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        ops.indexer_topk(st.cache, qi, w, st.block_table, st.seq_lens, st.q_start_loc, ws=bufs.ws,
-                         sel=bufs.sel, n_sel=bufs.n_sel)
-        ev[i][1].record(stream)
-        ops.sparse_attn_decode(st.cache, q, bufs.sel, bufs.n_sel, st.block_table, st.seq_lens,
-                               st.q_start_loc, n_splits, o_part=bufs.o_part, lse_part=bufs.lse_part)
-        ops.merge_splits(bufs.o_part, bufs.lse_part, out=bufs.out)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
+    step_ms = timed(g_step, args.steps)
+    torch.cuda.nvtx.range_pop()
     if world > 1:
         torch.distributed.barrier()
+    idx_ms = timed(g_idx, args.steps)
+    torch.cuda.synchronize()
     clk = clocks.stop()
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    idx_ms = [e[0].elapsed_time(e[1]) for e in ev]
     ms = float(np.mean(step_ms))
     t_idx = float(np.mean(idx_ms))
 
@@ -187,9 +223,6 @@ def run_gpu(args, rank, world, local_rank):
     h_sl = st.seq_lens.cpu().pin_memory()
     h_qsl = st.q_start_loc.cpu().pin_memory()
     h_out = torch.empty((T, 16, 128), dtype=torch.float32).pin_memory()
-    d_q, d_qi, d_w = torch.empty_like(q), torch.empty_like(qi), torch.empty_like(w)
-    d_bt, d_sl, d_qsl = (torch.empty_like(st.block_table), torch.empty_like(st.seq_lens),
-                         torch.empty_like(st.q_start_loc))
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qi, h_w, h_bt, h_sl, h_qsl))
     d2h = h_out.numel() * 4
     e2e_ms = []
@@ -197,10 +230,11 @@ def run_gpu(args, rank, world, local_rank):
         flush.fill_(float(i))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for d, h in ((d_q, h_q), (d_qi, h_qi), (d_w, h_w), (d_bt, h_bt), (d_sl, h_sl), (d_qsl, h_qsl)):
+        for d, h in ((q, h_q), (qi, h_qi), (w, h_w), (st.block_table, h_bt), (st.seq_lens, h_sl),
+                     (st.q_start_loc, h_qsl)):
             d.copy_(h, non_blocking=True)
-        out = ops.decode_step(st.cache, d_q, d_qi, d_w, d_bt, d_sl, d_qsl, bufs)
-        h_out.copy_(out, non_blocking=True)
+        g_step()
+        h_out.copy_(bufs.out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         if i >= args.warmup:
@@ -280,6 +314,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch kernels eagerly instead of CUDA graphs")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

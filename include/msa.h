@@ -77,6 +77,7 @@ typedef struct CUstream_st* msa_stream_t; /* same type as cudaStream_t */
 #define MSA_STATUS_BAD_PAGE 0x2       /* block_table entry outside the pool */
 #define MSA_STATUS_BAD_SEQ 0x4        /* n_q < 0, n_q > seq_len or seq_len > max_pages*128 */
 #define MSA_STATUS_BAD_SELECTION 0x8  /* a selected block id outside 0..r_j */
+#define MSA_STATUS_TIMEOUT 0x10       /* a bounded on-chip wait gave up (results invalid) */
 
 /* The KV cache and its metadata.  Caller-owned; the library only reads it. */
 typedef struct msa_cache {
@@ -129,9 +130,11 @@ int msa_quantize_kv_insert(const msa_cache* cache, const float* k, const float* 
  *               the lower id) in ascending order, then r_j; padded with -1.
  *   n_sel       int32 [n_q_total] out: min(topk, r_j) + 1.
  *   ws, ws_bytes scratch of at least msa_indexer_workspace_bytes(...) bytes.
- *               After the stream reaches the end of this call it holds the fp32
- *               block scores S[j][i] (row stride max_pages) for i < r_j;
- *               other entries are unspecified.
+ *               After the stream reaches the end of this call it holds, for
+ *               every query token j and block i < r_j, four fp32 partial maxima
+ *               P[j][i][0..3] (row stride 4 * max_pages floats): the maxima over
+ *               the block's token quarters; the block score is their max.  Other
+ *               entries are unspecified.
  * Block score S[j][i] = max over the 128 tokens t of block i of
  *   sum_h w[j][h] * max(0, q_idx[j][h] . key(t)), computed with fp32 sums of
  *   exact FP8 products.

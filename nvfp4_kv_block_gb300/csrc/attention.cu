@@ -70,17 +70,43 @@ __global__ void __launch_bounds__(kAttnThreads, 3) sparse_attn_kernel(AttnParams
   __shared__ uint2 s_tab[256];
   __shared__ float s_m[4][4], s_l[4][4];
   __shared__ float s_o[4][4][kHeadDim];
+  __shared__ int s_qsl[kMaxSeqs + 1];
+  __shared__ int s_blk[kSelStride], s_phys[kSelStride];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int split = blockIdx.x, kvh = blockIdx.y, j = blockIdx.z;
   build_dequant_table(s_tab, tid, kAttnThreads);
+  for (int i = tid; i <= p.n_seqs; i += kAttnThreads) s_qsl[i] = p.q_start_loc[i];
+  __syncthreads();
 
-  const int b = find_seq(p.q_start_loc, p.n_seqs, j);
-  const SeqInfo s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
+  const int b = find_seq(s_qsl, p.n_seqs, j);
+  const SeqInfo s = load_seq(b, p.seq_lens, s_qsl, p.max_pages, p.n_q_total);
   const bool seq_ok = s.ok && j >= s.q0 && j < s.q0 + s.n_q;
   const int pos = s.seq_len - s.n_q + (j - s.q0);
   const int r_blk = seq_ok ? pos / kPageTokens : -1;
+  pdl_wait();     // the selection comes from the top-k kernel
+  pdl_trigger();  // the merge kernel may launch and wait
   const int nsel = seq_ok ? min(p.n_sel[j], kSelStride) : 0;
+  // this split's block ids and physical pages, fetched once, all in parallel
+  if (tid < kSelStride) {
+    const int e = split + tid * p.n_splits;
+    int blk = -1, phys = -1;
+    if (e < nsel) {
+      blk = p.sel[(size_t)j * kSelStride + e];
+      if (blk < 0 || blk > r_blk) {
+        set_status(p.status, MSA_STATUS_BAD_SELECTION);
+        blk = -1;
+      } else {
+        phys = p.block_table[(size_t)b * p.max_pages + blk];
+        if (phys < 0 || phys >= p.n_pages) {
+          set_status(p.status, MSA_STATUS_BAD_PAGE);
+          phys = -1;
+        }
+      }
+    }
+    s_blk[tid] = blk;
+    s_phys[tid] = phys;
+  }
 
   // query fragments: column n = g holds query head 4*kvh + (g & 3); lane t owns
   // channels 32t..32t+31 -> b0 of k-step s = channels 32t+4s.., b1 = 32t+16+4s..
@@ -99,17 +125,9 @@ __global__ void __launch_bounds__(kAttnThreads, 3) sparse_attn_kernel(AttnParams
   const int tok_k = 32 * warp + 4 * g;  // K tokens of this lane: tok_k + i, i < 4
   const int tok_v = 32 * warp + 8 * t;  // V tokens of this lane: tok_v + i, i < 8
 
-  for (int e = split; e < nsel; e += p.n_splits) {
-    const int blk = p.sel[(size_t)j * kSelStride + e];
-    if (blk < 0 || blk > r_blk) {
-      if (tid == 0) set_status(p.status, MSA_STATUS_BAD_SELECTION);
-      continue;
-    }
-    const int phys = p.block_table[(size_t)b * p.max_pages + blk];
-    if (phys < 0 || phys >= p.n_pages) {
-      if (tid == 0) set_status(p.status, MSA_STATUS_BAD_PAGE);
-      continue;
-    }
+  for (int e = split, ei = 0; e < nsel; e += p.n_splits, ++ei) {
+    const int blk = s_blk[ei], phys = s_phys[ei];
+    if (phys < 0) continue;
     const int valid = blk == r_blk ? (pos % kPageTokens) + 1 : kPageTokens;
     const uint8_t* base = p.kv_pool + (size_t)phys * kKvPageBytes + kvh * kHeadBytes;
 
@@ -220,12 +238,15 @@ __global__ void __launch_bounds__(kAttnThreads, 3) sparse_attn_kernel(AttnParams
     for (int i = 0; i < 8; ++i) {
       const uint32_t sbyte = ((i < 4 ? vs.x : vs.y) >> (8 * (i & 3))) & 0xFF;
       const uint2 tb = s_tab[sbyte];
+      const uint2 d0 = dequant8(vc[i].x, tb), d1 = dequant8(vc[i].y, tb);
+      X[i][0] = d0.x; X[i][1] = d0.y; X[i][2] = d1.x; X[i][3] = d1.y;
+    }
+    if (valid < kPageTokens) {
       // masked tokens carry p = 0; their V bytes are zeroed so that stale NaN
       // codes or scales cannot reach the accumulators (0 * NaN = NaN)
-      const bool live = tok_v + i < valid;
-      const uint2 d0 = dequant8(vc[i].x, tb), d1 = dequant8(vc[i].y, tb);
-      X[i][0] = live ? d0.x : 0u; X[i][1] = live ? d0.y : 0u;
-      X[i][2] = live ? d1.x : 0u; X[i][3] = live ? d1.y : 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (tok_v + i >= valid) X[i][0] = X[i][1] = X[i][2] = X[i][3] = 0u;
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -296,6 +317,7 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(const float* __restrict
   const int row = blockIdx.x;  // j * n_heads + h
   const int j = row / n_heads, h = row % n_heads;
   const int ch = threadIdx.x;
+  pdl_wait();  // partials come from the attention kernel
   float M = -INFINITY;
   for (int sp = 0; sp < n_splits; ++sp)
     M = fmaxf(M, lse_part[((size_t)j * n_splits + sp) * n_heads + h]);
@@ -344,16 +366,14 @@ cudaError_t launch_sparse_attn(const msa_cache* c, const uint8_t* q, float softm
                 softmax_scale / c->s_enc_k * kLog2e, 1.0f / (256.0f * c->s_enc_v), o_part,
                 lse_part, c->status};
   dim3 grid(n_splits, kKvHeads, n_q_total);
-  sparse_attn_kernel<<<grid, kAttnThreads, 0, stream>>>(ap);
-  return cudaGetLastError();
+  return launch_pdl(sparse_attn_kernel, grid, dim3(kAttnThreads), 0, stream, ap);
 }
 
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int n_q_total, int n_heads,
                          int n_splits, float* out, cudaStream_t stream) {
   if (n_q_total == 0) return cudaSuccess;
-  merge_kernel<<<n_q_total * n_heads, kHeadDim, 0, stream>>>(o_part, lse_part, n_heads, n_splits,
-                                                            out);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3(n_q_total * n_heads), dim3(kHeadDim), 0, stream, o_part,
+                    lse_part, n_heads, n_splits, out);
 }
 
 cudaError_t launch_debug_fp8_page(const msa_cache* c, int64_t page, uint8_t* k8, uint8_t* v8,

@@ -5,24 +5,25 @@
 // scores the context, keeps 16 blocks plus the most recent one, and reads 128
 // index bytes per token.  Section "Parallelize index work across context":
 // splitting the scan keeps the selection exact (each block score is computed
-// once, by one warp, and the selection runs over all of them).
+// once, by one CTA, and the selection runs over all of them).
 //
-// Scan (hot loop): the pages to scan (blocks 0..r_last-1 of every sequence)
-// are flattened and cut into equal contiguous ranges, one per warp.  A warp
-// streams its pages 16 tokens at a time with 128-bit loads straight into
-// mma.sync fragments (tokens are the M dimension, the 8 indexer heads the N
-// dimension, the 128 dims the K dimension: 4 x m16n8k32 E4M3 MMAs per 16
-// tokens and query token), applies ReLU and the head weights on the fp32
-// accumulators, sums the heads with two quad shuffles and keeps the block max
-// in registers.  Only one fp32 per (query token, block) is written.
-//
-// Fragment mapping.  A page row (one token) holds 8 chunks of 16 dims,
-// chunk c stored at position c ^ (token & 7).  Lane (g = lane/4, t = lane%4)
-// loads chunks t and t+4 of tokens g and g+8 of the 16-token tile; word s of
-// chunk t (dims 16t+4s..16t+4s+3) is the A fragment of k-step s at k columns
-// 4t..4t+3, word s of chunk t+4 the one at columns 16+4t..16+4t+3.  The index
-// query uses the same dims -> (k-step, column) map, so the dot product is
-// unchanged.
+// Scan (hot loop), one persistent CTA per SM.  The pages to scan (blocks
+// 0..r_last-1 of every sequence) are flattened and cut into equal contiguous
+// ranges, one per CTA.  Warp-specialised pipeline:
+//   warp 0      TMA producer: one 16 KB cp.async.bulk per index page into an
+//               8-stage shared-memory ring (128 KB in flight per SM); also writes
+//               the index-query tile (B operand) of each sequence segment;
+//   warp 1      MMA issuer: per page, 4 x tcgen05.mma kind::f8f6f4 with M = 128
+//               tokens (the page, A from shared memory), N = 8 heads x query
+//               tokens (B), K = 128 dims, fp32 accumulators in tensor memory,
+//               double-buffered; tcgen05.commit frees the stage and hands the
+//               accumulator to the epilogue;
+//   warps 2-5   epilogue: tcgen05.ld of one token row per thread, ReLU, head
+//               weights, sum over heads, block max over the 128 rows; one fp32
+//               per (query token, block) is written.
+// The index page is stored pre-swizzled (chunk c of token t at chunk c ^ (t&7)),
+// which is exactly the 128-byte-swizzled K-major operand layout, so a plain
+// bulk copy lands it ready for the tensor core.
 #include "common.cuh"
 
 namespace msa {
@@ -39,22 +40,75 @@ struct ScanParams {
   const int* q_start_loc;
   int n_seqs;
   int n_q_total;
-  float* scores;  // [T][max_pages]
+  float* scores;  // [T][max_pages][4] partial block maxima
   int* status;
 };
 
-constexpr int kScanThreads = 128;
+constexpr int kScanThreads = 320;  // 10 warps
+constexpr int kStages = 8;
+constexpr int kNqMax = 8;                       // query tokens per pass
+constexpr int kBRows = kNqMax * kIdxHeads;      // 64
+constexpr int kBBytes = kBRows * kIdxDim;       // 8 KB
+constexpr int kAccs = 4;                        // accumulators in tensor memory
+constexpr int kTmemCols = kAccs * 64;           // 256 columns
+constexpr int kOffStages = 0;
+constexpr int kOffB = kStages * kIdxPageBytes;  // 131,072
+constexpr int kOffBars = kOffB + 2 * kBBytes;   // 147,456
+constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccs + 1;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kOffPrefix = kOffMisc + 16;
+
+size_t scan_smem_bytes(int n_seqs) { return 1024 + kOffPrefix + 4 * (size_t)(n_seqs + 1); }
 
 // Pages to scan for sequence b: blocks 0..r_last-1, r_last = (seq_len-1)/128.
 __device__ __forceinline__ int scan_pages(const SeqInfo& s) {
   return (s.ok && s.seq_len > 0 && s.n_q > 0) ? (s.seq_len - 1) / kPageTokens : 0;
 }
 
-template <int NQ>
-__global__ void __launch_bounds__(kScanThreads) indexer_scan_kernel(ScanParams p) {
-  __shared__ int s_prefix[kMaxSeqs + 1];
-  __shared__ int s_warp_sum[kScanThreads / 32];
+// Walks the segments (sequence, query-token group, page range) of the flattened
+// page range [pg, pg_end).  Every role of the CTA walks the same sequence.
+template <typename F>
+__device__ __forceinline__ void for_each_segment(const ScanParams& p, const int* s_prefix, long long pg,
+                                                 long long pg_end, F&& f) {
+  int lo = 0, hi = p.n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_prefix[mid] <= pg) lo = mid; else hi = mid - 1;
+  }
+  int b = lo;
+  while (pg < pg_end) {
+    while (s_prefix[b + 1] <= pg) ++b;
+    const SeqInfo s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
+    const int page0 = (int)(pg - s_prefix[b]);
+    const int page1 = (int)(min((long long)s_prefix[b + 1], pg_end) - s_prefix[b]);
+    for (int j0 = 0; j0 < s.n_q; j0 += kNqMax) {
+      if (!f(b, s, j0, min(kNqMax, s.n_q - j0), page0, page1)) return;
+    }
+    pg = s_prefix[b] + page1;
+    ++b;
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + kOffBars;
+  // barrier addresses
+  auto full = [&](int i) { return bar0 + 8 * i; };
+  auto empty = [&](int i) { return bar0 + 8 * (kStages + i); };
+  auto bfull = [&](int i) { return bar0 + 8 * (2 * kStages + i); };
+  auto bempty = [&](int i) { return bar0 + 8 * (2 * kStages + 2 + i); };
+  auto tfull = [&](int i) { return bar0 + 8 * (2 * kStages + 4 + i); };
+  auto tempty = [&](int i) { return bar0 + 8 * (2 * kStages + 4 + kAccs + i); };
+  const uint32_t done_bar = bar0 + 8 * (2 * kStages + 4 + 2 * kAccs);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* s_prefix = reinterpret_cast<int*>(smem + kOffPrefix);
+
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();     // inputs may come from the previous kernel in the stream
+  pdl_trigger();  // the top-k kernel may launch and run its prologue
 
   // -- exclusive prefix over sequences of the pages each one scans ------------
   {
@@ -63,7 +117,7 @@ __global__ void __launch_bounds__(kScanThreads) indexer_scan_kernel(ScanParams p
     int local = 0;
     for (int b = b0; b < b0 + per && b < p.n_seqs; ++b) {
       const SeqInfo s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
-      if (!s.ok) set_status(p.status, MSA_STATUS_BAD_SEQ);
+      if (!s.ok && blockIdx.x == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
       local += scan_pages(s);
     }
     int incl = local;
@@ -72,7 +126,25 @@ __global__ void __launch_bounds__(kScanThreads) indexer_scan_kernel(ScanParams p
       const int y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
+    __shared__ int s_warp_sum[kScanThreads / 32];
     if (lane == 31) s_warp_sum[warp] = incl;
+    if (tid == 0) {
+      for (int i = 0; i < kStages; ++i) {
+        mbar_init(full(i), 1);
+        mbar_init(empty(i), 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(bfull(i), 1);
+        mbar_init(bempty(i), 1);
+      }
+      for (int i = 0; i < kAccs; ++i) {
+        mbar_init(tfull(i), 1);
+        mbar_init(tempty(i), 4);
+      }
+      mbar_init(done_bar, 1);
+      *s_abort = 0;
+      fence_barrier_init();
+    }
     __syncthreads();
     int base = 0;
     for (int i = 0; i < warp; ++i) base += s_warp_sum[i];
@@ -82,133 +154,192 @@ __global__ void __launch_bounds__(kScanThreads) indexer_scan_kernel(ScanParams p
       run += scan_pages(load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total));
     }
     if (tid == kScanThreads - 1) s_prefix[p.n_seqs] = base + incl;
-    __syncthreads();
   }
+  if (warp == 1) tmem_alloc(smem_u32(s_tmem), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
   const long long total = s_prefix[p.n_seqs];
-  const long long gw = (long long)blockIdx.x * (kScanThreads / 32) + warp;
-  const long long nw = (long long)gridDim.x * (kScanThreads / 32);
-  long long pg = gw * total / nw;
-  const long long pg_end = (gw + 1) * total / nw;
-  if (pg >= pg_end) return;
+  const long long pg_begin = (long long)blockIdx.x * total / gridDim.x;
+  const long long pg_end = (long long)(blockIdx.x + 1) * total / gridDim.x;
 
-  const int g = lane >> 2, t = lane & 3;
-  // byte offsets, inside a 16-token tile, of this lane's four 16-byte loads
-  const int off_a0 = g * kIdxDim + ((t ^ g) << 4);        // token g,   chunk t
-  const int off_a1 = g * kIdxDim + (((t + 4) ^ g) << 4);  // token g,   chunk t+4
-  const int off_a2 = off_a0 + 8 * kIdxDim;                // token g+8, chunk t
-  const int off_a3 = off_a1 + 8 * kIdxDim;                // token g+8, chunk t+4
-
-  // sequence holding page pg
-  int b = 0;
-  {
-    int lo = 0, hi = p.n_seqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_prefix[mid] <= pg) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-  }
-  while (pg < pg_end) {
-    while (s_prefix[b + 1] <= pg) ++b;
-    const SeqInfo s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
-    const int page0 = (int)(pg - s_prefix[b]);
-    const int page1 = (int)(min((long long)s_prefix[b + 1], pg_end) - s_prefix[b]);
-    const int* bt = p.block_table + (size_t)b * p.max_pages;
-    for (int j0 = 0; j0 < s.n_q; j0 += NQ) {
-      const int nq = min(NQ, s.n_q - j0);
-      // index-query fragments and head weights of up to NQ query tokens
-      uint4 qb0[NQ], qb1[NQ];
-      float w0[NQ], w1[NQ];
-#pragma unroll
-      for (int jj = 0; jj < NQ; ++jj) {
-        const int tok = s.q0 + j0 + min(jj, nq - 1);
-        const uint8_t* qrow = p.q_idx + ((size_t)tok * kIdxHeads + g) * kIdxDim;
-        qb0[jj] = *reinterpret_cast<const uint4*>(qrow + 16 * t);
-        qb1[jj] = *reinterpret_cast<const uint4*>(qrow + 64 + 16 * t);
-        const float2 wv = *reinterpret_cast<const float2*>(p.w + (size_t)tok * kIdxHeads + 2 * t);
-        w0[jj] = wv.x;
-        w1[jj] = wv.y;
-      }
-      // stream tiles: 8 tiles of 16 tokens per page, one tile prefetched ahead
-      const int n_tiles = (page1 - page0) * 8;
-      auto tile_base = [&](int tile, bool& bad) -> const uint8_t* {
-        const int phys = bt[page0 + (tile >> 3)];
-        bad = phys < 0 || phys >= p.n_pages;
-        const int64_t pp = bad ? 0 : phys;
-        return p.idx_pool + pp * kIdxPageBytes + (tile & 7) * (16 * kIdxDim);
-      };
-      bool bad_cur;
-      const uint8_t* src = tile_base(0, bad_cur);
-      uint4 cur0 = ld_stream_v4(src + off_a0), cur1 = ld_stream_v4(src + off_a1);
-      uint4 cur2 = ld_stream_v4(src + off_a2), cur3 = ld_stream_v4(src + off_a3);
-      float bmax[NQ];
-#pragma unroll
-      for (int jj = 0; jj < NQ; ++jj) bmax[jj] = -INFINITY;
-      for (int tile = 0; tile < n_tiles; ++tile) {
-        uint4 nxt0 = cur0, nxt1 = cur1, nxt2 = cur2, nxt3 = cur3;
-        bool bad_nxt = false;
-        if (tile + 1 < n_tiles) {
-          const uint8_t* ns = tile_base(tile + 1, bad_nxt);
-          nxt0 = ld_stream_v4(ns + off_a0);
-          nxt1 = ld_stream_v4(ns + off_a1);
-          nxt2 = ld_stream_v4(ns + off_a2);
-          nxt3 = ld_stream_v4(ns + off_a3);
+  if (warp == 0) {
+    // ---------------- producer: index pages -----------------------------------
+    int it = 0;
+    for_each_segment(p, s_prefix, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
+      // block-table entries are fetched 32 at a time (one coalesced load per
+      // 32 pages, the next batch in flight) so that no dependent global load
+      // sits between two page copies
+      const int* bt = p.block_table + (size_t)b * p.max_pages;
+      int nxt = page0 + lane < page1 ? bt[page0 + lane] : 0;
+      for (int base = page0; base < page1; base += 32) {
+        const int cur = nxt;
+        nxt = base + 32 + lane < page1 ? bt[base + 32 + lane] : 0;
+        const int n = min(32, page1 - base);
+        for (int k = 0; k < n; ++k, ++it) {
+          const int st = it % kStages;
+          int phys = __shfl_sync(0xffffffffu, cur, k);
+          if (phys < 0 || phys >= p.n_pages) phys = 0;  // flagged by the epilogue
+          if (!mbar_wait(empty(st), ((it / kStages) & 1) ^ 1, s_abort)) return false;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full(st), kIdxPageBytes);
+            bulk_g2s(sbase + kOffStages + st * kIdxPageBytes, p.idx_pool + (size_t)phys * kIdxPageBytes,
+                     kIdxPageBytes, full(st));
+          }
+          __syncwarp();
         }
-        const uint32_t A0[4] = {cur0.x, cur0.y, cur0.z, cur0.w};
-        const uint32_t A1[4] = {cur1.x, cur1.y, cur1.z, cur1.w};
-        const uint32_t A2[4] = {cur2.x, cur2.y, cur2.z, cur2.w};
-        const uint32_t A3[4] = {cur3.x, cur3.y, cur3.z, cur3.w};
+      }
+      return true;
+    });
+    if (*s_abort) {
+      // drain: no bulk copy may still be writing shared memory when the CTA exits
+      for (int k = max(0, it - kStages); k < it; ++k) mbar_wait(full(k % kStages), (k / kStages) & 1, s_abort);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA warp: B tile of each segment, then the MMAs ----------
+    int it = 0, sg = 0;
+    for_each_segment(p, s_prefix, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
+      const int slot = sg & 1;
+      // the MMAs that read this slot two segments ago must be done
+      if (!mbar_wait(bempty(slot), ((sg >> 1) & 1) ^ 1, s_abort)) return false;
+      // index queries of tokens j0..j0+nq-1 -> rows (token, head), 128-byte
+      // swizzled K-major; rows up to the MMA's N are zero-padded
+      const int n_rows = 16 * ((nq + 1) >> 1);
+      uint8_t* bt_s = smem + kOffB + slot * kBBytes;
+      const uint8_t* qsrc = p.q_idx + (size_t)(s.q0 + j0) * kIdxHeads * kIdxDim;
 #pragma unroll
-        for (int jj = 0; jj < NQ; ++jj) {
+      for (int half = 0; half < 2; ++half) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int e = lane + 32 * (8 * half + u), row = e >> 3, c = e & 7;
+          v[u] = (row < nq * kIdxHeads) ? *reinterpret_cast<const uint4*>(qsrc + row * kIdxDim + c * 16)
+                                        : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int e = lane + 32 * (8 * half + u), row = e >> 3, c = e & 7;
+          if (row < n_rows) *reinterpret_cast<uint4*>(bt_s + row * kIdxDim + ((c ^ (row & 7)) << 4)) = v[u];
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      bool ok = true;
+      if (lane == 0) {
+        const uint32_t idesc = umma_idesc_e4m3(128, n_rows);
+        const uint64_t bdesc = umma_desc_sw128(sbase + kOffB + slot * kBBytes);
+        for (int page = page0; page < page1; ++page, ++it) {
+          const int st = it % kStages, acc = it % kAccs;
+          if (!mbar_wait(full(st), (it / kStages) & 1, s_abort)) { ok = false; break; }
+          if (!mbar_wait(tempty(acc), ((it / kAccs) & 1) ^ 1, s_abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t adesc = umma_desc_sw128(sbase + kOffStages + st * kIdxPageBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)  // K = 32 bytes per MMA: +32 B = +2 in the encoded address
+            umma_e4m3(tmem + acc * 64, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0);
+          umma_commit(empty(st));
+          umma_commit(tfull(acc));
+        }
+        if (ok) umma_commit(bempty(slot));
+      }
+      ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+      it = __shfl_sync(0xffffffffu, it, 0);
+      ++sg;
+      return ok;
+    });
+    if (lane == 0 && *s_abort) {
+      // no tcgen05.mma may still be running when tensor memory is released
+      volatile int ignore = 0;
+      umma_commit(done_bar);
+      mbar_wait(done_bar, 0, &ignore);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: two sets of four warps, set = page parity ------
+    // warps 2..5 and 6..9 -> TMEM lane quadrants 2,3,0,1; each warp writes the
+    // max over its 32 token rows, the top-k kernel takes the max of the four.
+    const int quad = warp & 3, set = (warp - 2) >> 2;
+    int it = 0;
+    for_each_segment(p, s_prefix, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
+      float wr[kNqMax][kIdxHeads];
+#pragma unroll
+      for (int jj = 0; jj < kNqMax; ++jj)
+#pragma unroll
+        for (int h = 0; h < kIdxHeads; ++h)
+          wr[jj][h] = jj < nq ? p.w[(size_t)(s.q0 + j0 + jj) * kIdxHeads + h] : 0.f;
+      const int* bt = p.block_table + (size_t)b * p.max_pages;
+      float* srow = p.scores + ((size_t)(s.q0 + j0 + lane) * p.max_pages) * 4 + quad;
+      int bt_nxt = page0 + lane < page1 ? bt[page0 + lane] : 0;
+      int bt_cur = 0;
+      for (int page = page0; page < page1; ++page, ++it) {
+        if (((page - page0) & 31) == 0) {  // block-table entries 32 at a time
+          bt_cur = bt_nxt;
+          bt_nxt = page + 32 + lane < page1 ? bt[page + 32 + lane] : 0;
+        }
+        const int phys = __shfl_sync(0xffffffffu, bt_cur, (page - page0) & 31);
+        if ((it & 1) != set) continue;
+        const int acc = it % kAccs;
+        if (!mbar_wait(tfull(acc), (it / kAccs) & 1, s_abort)) return false;
+        tc_fence_after();
+        float m[kNqMax];
+#pragma unroll
+        for (int c = 0; c < kNqMax / 2; ++c) {
+          if (2 * c < nq) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * quad) << 16) + acc * 64 + 16 * c, v);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              float sc = 0.f;
+#pragma unroll
+              for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[2 * c + u][h], fmaxf(v[8 * u + h], 0.f), sc);
+              m[2 * c + u] = sc;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(acc));
+        float mine = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < kNqMax; ++jj) {
           if (jj < nq) {
-            const uint32_t B0[4] = {qb0[jj].x, qb0[jj].y, qb0[jj].z, qb0[jj].w};
-            const uint32_t B1[4] = {qb1[jj].x, qb1[jj].y, qb1[jj].z, qb1[jj].w};
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            // a0: token g dims of chunk t; a1: token g+8 chunk t; a2: token g chunk t+4; a3: token g+8 chunk t+4
+            float x = m[jj];
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) mma_e4m3(acc, A0[ks], A2[ks], A1[ks], A3[ks], B0[ks], B1[ks]);
-            // rows g, g+8 (tokens); columns 2t, 2t+1 (heads)
-            float v0 = fmaf(w1[jj], fmaxf(acc[1], 0.f), w0[jj] * fmaxf(acc[0], 0.f));
-            float v1 = fmaf(w1[jj], fmaxf(acc[3], 0.f), w0[jj] * fmaxf(acc[2], 0.f));
-            v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
-            v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-            v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
-            v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
-            bmax[jj] = fmaxf(bmax[jj], fmaxf(v0, v1));
+            for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+            if (lane == jj) mine = x;
           }
         }
-        if ((tile & 7) == 7) {
-          const int page = page0 + (tile >> 3);
-#pragma unroll
-          for (int jj = 0; jj < NQ; ++jj) {
-            float m = bmax[jj];
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-            if (lane == jj && jj < nq)
-              p.scores[(size_t)(s.q0 + j0 + jj) * p.max_pages + page] = bad_cur ? -INFINITY : m;
-            bmax[jj] = -INFINITY;
-          }
-          if (bad_cur && lane == 0) set_status(p.status, MSA_STATUS_BAD_PAGE);
+        if (lane < nq) {
+          const bool bad = phys < 0 || phys >= p.n_pages;
+          if (bad && lane == 0 && quad == 0) set_status(p.status, MSA_STATUS_BAD_PAGE);
+          srow[(size_t)page * 4] = bad ? -INFINITY : mine;
         }
-        cur0 = nxt0; cur1 = nxt1; cur2 = nxt2; cur3 = nxt3;
-        bad_cur = bad_nxt;
       }
-    }
-    pg = s_prefix[b] + page1;
-    ++b;
+      return true;
+    });
   }
+
+  // ---------------- teardown -------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid == 0 && *s_abort) set_status(p.status, MSA_STATUS_TIMEOUT);
 }
 
 // ---------------------------------------------------------------------------
 // Top-16 + recent per query token.  Keys are (ordered score << 32) | ~block,
-// unique, larger = better (higher score, then lower block).  256 threads:
-// each takes the max key of its strided blocks; the 16th largest of those 256
-// maxima, theta, is a lower bound of the 16th largest key overall (the 16
-// largest maxima are 16 distinct keys), so every winner has key >= theta.  The
-// few candidates >= theta are ranked exactly by counting.
+// unique, larger = better (higher score, then lower block).  256 threads in 16
+// half-warps; half-warp h owns the blocks with (block & 15) == h.  The
+// smallest of the 16 half-warp maxima, theta, is the smallest of 16 distinct
+// keys, hence <= the 16th largest key: every winner has key >= theta.  The few
+// candidates >= theta are ranked exactly by counting.
 constexpr int kTopkThreads = 256;
-constexpr int kMaxCand = 4096;
+constexpr int kMaxCand = 2048;
 
 struct TopkParams {
   const float* scores;
@@ -222,21 +353,33 @@ struct TopkParams {
   int* status;
 };
 
+// Block score = max of the four partial maxima the scan wrote for block blk.
 __device__ __forceinline__ unsigned long long block_key(const float* row, int blk) {
-  return ((unsigned long long)ordered_bits(row[blk]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
+  const float4 q = reinterpret_cast<const float4*>(row)[blk];
+  const float sc = fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w));
+  return ((unsigned long long)ordered_bits(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
-  __shared__ unsigned long long s_key[kTopkThreads];
+  __shared__ int s_qsl[kMaxSeqs + 1];
+  __shared__ unsigned long long s_hmax[16];
   __shared__ unsigned long long s_cand[kMaxCand];
+  __shared__ unsigned long long s_red[kTopkThreads / 32];
   __shared__ int s_win[kTopK];
-  __shared__ unsigned long long s_theta;
   __shared__ int s_ncand;
-  const int j = blockIdx.x, tid = threadIdx.x;
-  const int b = find_seq(p.q_start_loc, p.n_seqs, j);
-  const SeqInfo s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
+  const int j = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i <= p.n_seqs; i += kTopkThreads) s_qsl[i] = p.q_start_loc[i];
+  __syncthreads();
+  const int b = find_seq(s_qsl, p.n_seqs, j);
+  const SeqInfo s = load_seq(b, p.seq_lens, s_qsl, p.max_pages, p.n_q_total);
   int* out = p.sel + (size_t)j * kSelStride;
   if (!s.ok || j < s.q0 || j >= s.q0 + s.n_q) {
+    pdl_wait();
+    pdl_trigger();
     if (tid == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
     if (tid < kSelStride) out[tid] = -1;
     if (tid == 0) p.n_sel[j] = 0;
@@ -244,26 +387,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
   }
   const int pos = s.seq_len - s.n_q + (j - s.q0);
   const int r = pos / kPageTokens;
-  const float* row = p.scores + (size_t)j * p.max_pages;
+  const float* row = p.scores + (size_t)j * p.max_pages * 4;
+  pdl_wait();     // block scores come from the scan kernel
   if (r <= kTopK) {
+    pdl_trigger();
     if (tid < kSelStride) out[tid] = tid <= r ? tid : -1;
     if (tid == 0) p.n_sel[j] = r + 1;
     return;
   }
+  // thread t owns blocks base, base + 256, ... with base & 15 == t / 16
+  const int base = ((tid & 15) << 4) | (tid >> 4);
   unsigned long long mykey = 0;
-  for (int blk = tid; blk < r; blk += kTopkThreads) {
-    const unsigned long long k = block_key(row, blk);
-    mykey = k > mykey ? k : mykey;
-  }
-  s_key[tid] = mykey;
+#pragma unroll 4
+  for (int blk = base; blk < r; blk += kTopkThreads) mykey = umax64(mykey, block_key(row, blk));
+#pragma unroll
+  for (int o = 8; o; o >>= 1) mykey = umax64(mykey, __shfl_xor_sync(0xffffffffu, mykey, o));
+  if ((lane & 15) == 0) s_hmax[tid >> 4] = mykey;
   if (tid == 0) s_ncand = 0;
   __syncthreads();
-  int rank = 0;
-  for (int i = 0; i < kTopkThreads; ++i) rank += s_key[i] > mykey;
-  if (rank == kTopK - 1) s_theta = mykey;
-  __syncthreads();
-  const unsigned long long theta = s_theta;
-  for (int blk = tid; blk < r; blk += kTopkThreads) {
+  unsigned long long theta = s_hmax[0];
+#pragma unroll
+  for (int i = 1; i < 16; ++i) theta = s_hmax[i] < theta ? s_hmax[i] : theta;
+#pragma unroll 4
+  for (int blk = base; blk < r; blk += kTopkThreads) {
     const unsigned long long k = block_key(row, blk);
     if (k >= theta) {
       const int slot = atomicAdd(&s_ncand, 1);
@@ -271,12 +417,35 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
     }
   }
   __syncthreads();
-  const int nc = min(s_ncand, kMaxCand);
-  for (int c = tid; c < nc; c += kTopkThreads) {
-    const unsigned long long k = s_cand[c];
-    int rk = 0;
-    for (int i = 0; i < nc; ++i) rk += s_cand[i] > k;
-    if (rk < kTopK) s_win[rk] = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFu));
+  const int nc = s_ncand;
+  if (nc <= kMaxCand) {
+    for (int c = tid; c < nc; c += kTopkThreads) {
+      const unsigned long long k = s_cand[c];
+      int rk = 0;
+      for (int i = 0; i < nc; ++i) rk += s_cand[i] > k;
+      if (rk < kTopK) s_win[rk] = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFu));
+    }
+  } else {
+    // too many candidates for the buffer (adversarial score layouts): 16 rounds
+    // of block-wide argmax, each over the keys below the previous winner
+    unsigned long long bound = ~0ull;
+    for (int k = 0; k < kTopK; ++k) {
+      unsigned long long best = 0;
+      for (int blk = tid; blk < r; blk += kTopkThreads) {
+        const unsigned long long key = block_key(row, blk);
+        if (key < bound) best = umax64(best, key);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+      if (lane == 0) s_red[warp] = best;
+      __syncthreads();
+      best = s_red[0];
+#pragma unroll
+      for (int i = 1; i < kTopkThreads / 32; ++i) best = umax64(best, s_red[i]);
+      if (tid == 0) s_win[k] = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+      bound = best;
+      __syncthreads();
+    }
   }
   __syncthreads();
   if (tid < kTopK) {
@@ -290,6 +459,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
     out[kTopK] = r;
     p.n_sel[j] = kTopK + 1;
   }
+  pdl_trigger();  // the attention kernel may launch now (it waits for this grid to finish)
 }
 
 }  // namespace
@@ -301,16 +471,28 @@ cudaError_t launch_indexer_topk(const msa_cache* c, const uint8_t* q_idx, const 
   if (n_q_total == 0 || n_seqs == 0) return cudaSuccess;
   ScanParams sp{static_cast<const uint8_t*>(c->idx_pool), c->n_pages, q_idx, w, block_table,
                 max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, scores, c->status};
-  const int blocks = 152 * 8;
-  if (n_q_total == n_seqs)
-    indexer_scan_kernel<1><<<blocks, kScanThreads, 0, stream>>>(sp);
-  else
-    indexer_scan_kernel<8><<<blocks, kScanThreads, 0, stream>>>(sp);
-  cudaError_t e = cudaGetLastError();
+  // per-device launch set-up, done once (not a stream operation, so a later call
+  // may be captured into a CUDA graph)
+  static int s_n_sm[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (s_n_sm[dev] == 0) {
+    int n_sm = 0;
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(indexer_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)scan_smem_bytes(kMaxSeqs));
+    if (e != cudaSuccess) return e;
+    s_n_sm[dev] = n_sm;
+  }
+  const int n_sm = s_n_sm[dev];
+  const size_t smem = scan_smem_bytes(n_seqs);
+  e = launch_pdl(indexer_scan_kernel, dim3(n_sm), dim3(kScanThreads), smem, stream, sp);
   if (e != cudaSuccess) return e;
   TopkParams tp{scores, max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, sel, n_sel, c->status};
-  topk_kernel<<<n_q_total, kTopkThreads, 0, stream>>>(tp);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3(n_q_total), dim3(kTopkThreads), 0, stream, tp);
 }
 
 }  // namespace msa

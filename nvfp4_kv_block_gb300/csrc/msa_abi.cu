@@ -53,7 +53,7 @@ int msa_quantize_kv_insert(const msa_cache* cache, const float* k, const float* 
 
 size_t msa_indexer_workspace_bytes(int32_t n_q_total, int32_t max_pages) {
   if (n_q_total <= 0 || max_pages <= 0) return 256;
-  const size_t b = (size_t)n_q_total * (size_t)max_pages * sizeof(float);
+  const size_t b = (size_t)n_q_total * (size_t)max_pages * 4 * sizeof(float);
   return (b + 255) / 256 * 256;
 }
 

@@ -191,8 +191,10 @@ def indexer_topk(cache, q_idx, w, block_table, seq_lens, q_start_loc, ws=None, s
 
 
 def block_scores_view(ws, n_q_total, max_pages):
-    """The fp32 block scores S[T, max_pages] held in the indexer workspace."""
-    return ws[: n_q_total * max_pages * 4].view(torch.float32).view(n_q_total, max_pages)
+    """The fp32 block scores S[T, max_pages]: max of the four partial maxima per
+    block held in the indexer workspace (valid for blocks < r_j)."""
+    part = ws[: n_q_total * max_pages * 16].view(torch.float32).view(n_q_total, max_pages, 4)
+    return part.amax(dim=-1)
 
 
 def sparse_attn_decode(cache, q, sel, n_sel, block_table, seq_lens, q_start_loc, n_splits,
