@@ -14,6 +14,9 @@ cudaError_t launch_indexer_topk(const msa_cache*, const uint8_t*, const float*, 
 cudaError_t launch_sparse_attn(const msa_cache*, const uint8_t*, float, const int*, const int*,
                                const int*, int, const int*, const int*, int, int, int, float*,
                                float*, cudaStream_t);
+cudaError_t launch_sparse_attn_tc(const msa_cache*, const uint8_t*, float, const int*, const int*,
+                                  const int*, int, const int*, const int*, int, int, int, float*,
+                                  float*, cudaStream_t);
 cudaError_t launch_merge(const float*, const float*, int, int, int, float*, cudaStream_t);
 cudaError_t launch_debug_fp8_page(const msa_cache*, int64_t, uint8_t*, uint8_t*, cudaStream_t);
 }  // namespace msa
@@ -96,7 +99,7 @@ int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q
                         !o_part || !lse_part || n_seqs == 0))
     return MSA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(q) & 15) return MSA_ERR_INVALID_ARG;
-  return launched(msa::launch_sparse_attn(cache, q, softmax_scale, sel, n_sel, block_table,
+  return launched(msa::launch_sparse_attn_tc(cache, q, softmax_scale, sel, n_sel, block_table,
                                           max_pages, seq_lens, q_start_loc, n_seqs, n_q_total,
                                           n_splits, o_part, lse_part,
                                           reinterpret_cast<cudaStream_t>(stream)));
