@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_attn_tc_kernel(AttnParams 
   // zero the Q/P tile (rows 4-7 and 16-23 stay zero; Q and P rows are written below)
   for (int i = tid; i < 24 * 128 / 16; i += kThreads) reinterpret_cast<uint4*>(qp)[i] = make_uint4(0, 0, 0, 0);
   if (warp == 0) tmem_alloc(smem_u32(s_tmem), kTmemCols);
+  __syncthreads();  // s_seq = -1 is in place before any thread records a match
   // sequence of token j: the b with q_start_loc[b] <= j < q_start_loc[b+1]
   for (int base = 0; base < p.n_seqs; base += kThreads) {
     const int b = base + tid;

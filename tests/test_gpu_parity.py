@@ -186,6 +186,9 @@ def test_full_size_config_sampled(cfg):
     rng = np.random.default_rng(1000 + cfg)
     tokens = sorted(set([0, T // 2, T - 1] + [int(x) for x in rng.integers(0, T, 2)]))
     _check_tokens(wl, side, bufs, out, S, tokens)
+    # every token (not only the sampled ones) got a finite, non-empty output
+    assert np.isfinite(out).all()
+    assert (np.abs(out).reshape(T, -1).max(axis=1) > 0).all()
     # sampled pages bit-exact, including the partial last page of a sequence
     kv = st.cache.kv_pool
     ip = st.cache.idx_pool
