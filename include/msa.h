@@ -71,6 +71,10 @@ typedef struct CUstream_st* msa_stream_t; /* same type as cudaStream_t */
 #define MSA_ERR_UNSUPPORTED_SHAPE (-2)
 #define MSA_ERR_WORKSPACE_TOO_SMALL (-3)
 #define MSA_ERR_LAUNCH_FAILED (-4)    /* a kernel launch returned an error */
+#define MSA_ERR_SCRATCH_CAPACITY (-5) /* msa_indexer_topk_noalloc: shape beyond its static scratch */
+
+/* Bytes of the static scratch behind msa_indexer_topk_noalloc. */
+#define MSA_INDEXER_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
 /* Sticky device status bits (OR-ed into *msa_cache.status). */
 #define MSA_STATUS_BAD_SLOT 0x1       /* slot_mapping points outside the pool */
@@ -148,6 +152,35 @@ int msa_indexer_topk(const msa_cache* cache, const uint8_t* q_idx, const float* 
 
 /* Bytes of scratch msa_indexer_topk needs (a multiple of 256). */
 size_t msa_indexer_workspace_bytes(int32_t n_q_total, int32_t max_pages);
+
+/*
+ * msa_indexer_topk without a workspace argument, for callers that cannot
+ * allocate device memory: code that runs inside a host framework which owns
+ * every device allocation, real-time decode loops where a cudaMalloc (which
+ * may synchronise the device) is not allowed between steps, or plug-ins that
+ * receive only their input and output buffers.  The pages have no counterpart
+ * of this call; it is a deployment convenience.
+ *
+ * Same arguments, results and errors as msa_indexer_topk minus ws/ws_bytes.
+ * The scratch is a file-scope device array of MSA_INDEXER_NOALLOC_SCRATCH_BYTES
+ * (8 MiB) inside the library; every GPU that loads the library keeps it until
+ * the process exits.  Shapes that need more, i.e.
+ * msa_indexer_workspace_bytes(n_q_total, max_pages) > that capacity, return
+ * MSA_ERR_SCRATCH_CAPACITY and enqueue nothing.  Nothing in the array needs
+ * clearing: every entry a call reads was written earlier by that same call.
+ * The array is shared by all calls on a device and keeps the last call's
+ * contents, so calls whose kernels overlap on the GPU (e.g. on two streams
+ * without ordering) race and must not be issued.  The first call on each
+ * device looks up the array's device address (with that device current);
+ * make that first call before any stream capture.  No cudaMalloc, cudaFree
+ * or allocating routine is called.
+ */
+int msa_indexer_topk_noalloc(const msa_cache* cache, const uint8_t* q_idx, const float* w,
+                             int32_t n_idx_heads, const int32_t* block_table, int32_t max_pages,
+                             const int32_t* seq_lens, const int32_t* q_start_loc, int32_t n_seqs,
+                             int32_t n_q_total, int32_t topk, int32_t* sel, int32_t* n_sel,
+                             msa_stream_t stream);
+
 
 /*
  * Split-context sparse GQA attention over the selected blocks (blog, "Sparse

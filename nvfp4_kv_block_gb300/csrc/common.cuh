@@ -28,6 +28,8 @@ constexpr int kIdxPageBytes = kPageTokens * kIdxDim;  // 16,384
 constexpr int kOffKc = 0, kOffKs = 8192, kOffVc = 9216, kOffVs = 17408;
 constexpr int kMaxSeqs = 4096;
 constexpr int kMaxSplits = 64;
+// Capacity of the file-scope scratch of msa_indexer_topk_noalloc.
+constexpr size_t kStaticScratchBytes = MSA_INDEXER_NOALLOC_SCRATCH_BYTES;
 
 __device__ __forceinline__ void set_status(int* status, int bits) {
   if (status) atomicOr(status, bits);

@@ -24,6 +24,8 @@
 // The index page is stored pre-swizzled (chunk c of token t at chunk c ^ (t&7)),
 // which is exactly the 128-byte-swizzled K-major operand layout, so a plain
 // bulk copy lands it ready for the tensor core.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace msa {
@@ -493,6 +495,45 @@ cudaError_t launch_indexer_topk(const msa_cache* c, const uint8_t* q_idx, const 
   if (e != cudaSuccess) return e;
   TopkParams tp{scores, max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, sel, n_sel, c->status};
   return launch_pdl(topk_kernel, dim3(n_q_total), dim3(kTopkThreads), 0, stream, tp);
+}
+
+}  // namespace msa
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the indexer call.  Its scratch (the partial block
+// maxima) lives in a file-scope device array instead of a caller workspace.
+// Every GPU that loads the library holds this array until the process exits.
+static __device__ __align__(256) float g_static_scores[msa::kStaticScratchBytes / sizeof(float)];
+
+namespace msa {
+namespace {
+std::mutex g_static_mu;
+float* g_static_ptr[64] = {nullptr};  // device address of g_static_scores, per device
+}  // namespace
+
+cudaError_t launch_indexer_topk_noalloc(const msa_cache* c, const uint8_t* q_idx, const float* w,
+                                        const int* block_table, int max_pages, const int* seq_lens,
+                                        const int* q_start_loc, int n_seqs, int n_q_total, int* sel,
+                                        int* n_sel, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  float* scratch = nullptr;
+  {
+    // One-time set-up per device, with that device current: the host-side
+    // symbol is only a stand-in, the kernels need the device address.
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_static_scores);
+      if (e != cudaSuccess) return e;
+      g_static_ptr[dev] = static_cast<float*>(ptr);
+    }
+    scratch = g_static_ptr[dev];
+  }
+  return launch_indexer_topk(c, q_idx, w, block_table, max_pages, seq_lens, q_start_loc, n_seqs,
+                             n_q_total, sel, n_sel, scratch, stream);
 }
 
 }  // namespace msa

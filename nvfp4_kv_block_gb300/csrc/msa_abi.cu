@@ -11,6 +11,9 @@ cudaError_t launch_absmax(const float*, int64_t, float*, cudaStream_t);
 cudaError_t launch_indexer_topk(const msa_cache*, const uint8_t*, const float*, const int*, int,
                                 const int*, const int*, int, int, int*, int*, float*,
                                 cudaStream_t);
+cudaError_t launch_indexer_topk_noalloc(const msa_cache*, const uint8_t*, const float*, const int*,
+                                        int, const int*, const int*, int, int, int*, int*,
+                                        cudaStream_t);
 cudaError_t launch_sparse_attn(const msa_cache*, const uint8_t*, float, const int*, const int*,
                                const int*, int, const int*, const int*, int, int, int, float*,
                                float*, cudaStream_t);
@@ -81,6 +84,27 @@ int msa_indexer_topk(const msa_cache* cache, const uint8_t* q_idx, const float* 
                                            q_start_loc, n_seqs, n_q_total, sel, n_sel,
                                            static_cast<float*>(ws),
                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_indexer_topk_noalloc(const msa_cache* cache, const uint8_t* q_idx, const float* w,
+                             int32_t n_idx_heads, const int32_t* block_table, int32_t max_pages,
+                             const int32_t* seq_lens, const int32_t* q_start_loc, int32_t n_seqs,
+                             int32_t n_q_total, int32_t topk, int32_t* sel, int32_t* n_sel,
+                             msa_stream_t stream) {
+  if (int rc = check_cache(cache)) return rc;
+  if (n_idx_heads != msa::kIdxHeads || topk != msa::kTopK) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_seqs < 0 || n_q_total < 0 || max_pages <= 0) return MSA_ERR_INVALID_ARG;
+  if (n_seqs > msa::kMaxSeqs || max_pages > kMaxPagesPerSeq) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_q_total > 0 && (!q_idx || !w || !block_table || !seq_lens || !q_start_loc || !sel ||
+                        !n_sel || n_seqs == 0))
+    return MSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_idx) & 15) || (reinterpret_cast<uintptr_t>(w) & 7))
+    return MSA_ERR_INVALID_ARG;
+  if (msa_indexer_workspace_bytes(n_q_total, max_pages) > MSA_INDEXER_NOALLOC_SCRATCH_BYTES)
+    return MSA_ERR_SCRATCH_CAPACITY;
+  return launched(msa::launch_indexer_topk_noalloc(cache, q_idx, w, block_table, max_pages,
+                                                   seq_lens, q_start_loc, n_seqs, n_q_total, sel,
+                                                   n_sel, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q_heads,
@@ -155,6 +179,7 @@ const char* msa_status_string(int code) {
     case MSA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
     case MSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case MSA_ERR_LAUNCH_FAILED: return "kernel launch failed";
+    case MSA_ERR_SCRATCH_CAPACITY: return "larger than the library's static scratch";
     case MSA_STATUS_BAD_SLOT: return "device: slot outside the pool";
     case MSA_STATUS_BAD_PAGE: return "device: block table entry outside the pool";
     case MSA_STATUS_BAD_SEQ: return "device: inconsistent sequence lengths / query counts";

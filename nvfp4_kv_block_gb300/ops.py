@@ -26,10 +26,11 @@ IDX_HEADS = 8
 Q_HEADS = 16
 TOPK = 16
 KV_PAGE_BYTES = 73_728
+NOALLOC_SCRATCH_BYTES = 8 << 20  # MSA_INDEXER_NOALLOC_SCRATCH_BYTES
 IDX_PAGE_BYTES = 16_384
 
 ERRORS = {-1: "invalid argument", -2: "unsupported shape", -3: "workspace too small",
-          -4: "kernel launch failed"}
+          -4: "kernel launch failed", -5: "larger than the library's static scratch"}
 
 
 class MsaError(RuntimeError):
@@ -60,6 +61,8 @@ _SIGS = {
     "msa_indexer_topk": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _P,
                                         _P, _P, ctypes.c_size_t, _P]),
     "msa_indexer_workspace_bytes": (ctypes.c_size_t, [_I32, _I32]),
+    "msa_indexer_topk_noalloc": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32,
+                                                _P, _P, _P]),
     "msa_sparse_attn_decode": (ctypes.c_int, [_P, _P, _I32, ctypes.c_float, _P, _P, _P, _I32, _P,
                                               _P, _I32, _I32, _I32, _P, _P, _P]),
     "msa_merge_splits": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P]),
@@ -188,6 +191,30 @@ def indexer_topk(cache, q_idx, w, block_table, seq_lens, q_start_loc, ws=None, s
         _ptr(q_start_loc, torch.int32, "q_start_loc"), n_seqs, T, topk, _ptr(sel, torch.int32, "sel"),
         _ptr(n_sel, torch.int32, "n_sel"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()))
     return sel, n_sel, ws
+
+
+def indexer_topk_noalloc(cache, q_idx, w, block_table, seq_lens, q_start_loc, sel=None,
+                         n_sel=None, topk=TOPK):
+    """indexer_topk through the allocation-free entry point (static scratch in the
+    library).  Returns (sel [T,17], n_sel [T])."""
+    T = q_idx.shape[0]
+    if tuple(q_idx.shape) != (T, IDX_HEADS, IDX_DIM) or tuple(w.shape) != (T, IDX_HEADS):
+        raise ValueError("q_idx must be [T, 8, 128] uint8 and w [T, 8] float32")
+    n_seqs, max_pages = block_table.shape
+    if tuple(seq_lens.shape) != (n_seqs,) or tuple(q_start_loc.shape) != (n_seqs + 1,):
+        raise ValueError("seq_lens must be [B], q_start_loc [B+1]")
+    dev = q_idx.device
+    if sel is None:
+        sel = torch.empty((T, topk + 1), dtype=torch.int32, device=dev)
+    if n_sel is None:
+        n_sel = torch.empty((T,), dtype=torch.int32, device=dev)
+    c = cache.struct()
+    _check(lib().msa_indexer_topk_noalloc(
+        ctypes.byref(c), _ptr(q_idx, torch.uint8, "q_idx"), _ptr(w, torch.float32, "w"), IDX_HEADS,
+        _ptr(block_table, torch.int32, "block_table"), max_pages, _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(q_start_loc, torch.int32, "q_start_loc"), n_seqs, T, topk, _ptr(sel, torch.int32, "sel"),
+        _ptr(n_sel, torch.int32, "n_sel"), _stream()))
+    return sel, n_sel
 
 
 def block_scores_view(ws, n_q_total, max_pages):

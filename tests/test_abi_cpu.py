@@ -80,3 +80,18 @@ def test_host_validation_needs_no_gpu(lib):
     assert lib.msa_merge_splits(fake, fake, 1, 16, 0, fake, None) == -1
     assert lib.msa_debug_fp8_page(ctypes.byref(c), 5, fake, fake, None) == -1
     assert lib.msa_status_string(-3) == b"workspace too small"
+
+
+def test_noalloc_entry_point_rejects_shapes_beyond_its_scratch(lib):
+    # 16 bytes of scratch per (query token, block): 16 tokens x 65,536 blocks needs
+    # 16 MiB, beyond the 8 MiB static array; rejected before any CUDA call
+    P = ctypes.c_void_p
+    fake = P(16)
+    c = _cache()
+    assert 16 * 65536 * 16 > ops.NOALLOC_SCRATCH_BYTES
+    rc = lib.msa_indexer_topk_noalloc(ctypes.byref(c), fake, fake, 8, fake, 65536, fake, fake, 1, 16,
+                                      16, fake, fake, None)
+    assert rc == -5
+    assert lib.msa_status_string(-5) == b"larger than the library's static scratch"
+    # the largest shape of the workloads here fits: 297 tokens x 1,680 blocks
+    assert ops.indexer_workspace_bytes(297, 1680) <= ops.NOALLOC_SCRATCH_BYTES
