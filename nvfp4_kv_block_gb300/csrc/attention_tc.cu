@@ -68,12 +68,6 @@ struct AttnParams {
   int* status;
 };
 
-// fp32 <-> order-preserving uint32 for redux max
-__device__ __forceinline__ uint32_t f2ord(float f) { return ordered_bits(f); }
-__device__ __forceinline__ float ord2f(uint32_t u) {
-  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
-}
-
 // Converts half a token row -- 32 code bytes = channels 64*hh..64*hh+63, groups
 // 4*hh..4*hh+3 -- to 64 FP8 bytes and stores them into row `row` of a
 // 128-byte-swizzled tile (16-byte chunk c at position c ^ (row & 7)).
@@ -231,9 +225,9 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_attn_tc_kernel(AttnParams 
     const int valid = s_blk[e] == r_blk ? (pos % kPageTokens) + 1 : kPageTokens;
     const bool live = tok < valid;
     const uint8_t* raw = smem + kOffRaw + (e & 1) * kHeadBytes;
-    if (tid == 0) mbar_wait(bar_raw0 + 8 * (e & 1), (e >> 1) & 1, s_abort);
-    __syncthreads();
-    if (*s_abort) break;
+    // every thread waits for the page itself (a timeout only raises s_abort; the
+    // next CTA barrier turns it into a uniform exit)
+    mbar_wait(bar_raw0 + 8 * (e & 1), (e >> 1) & 1, s_abort);
     // ---- K -> FP8 tile (the previous page's PV MMA only reads V and P) ------------
     dequant_half_row(raw + kOffKc + tok * 64, raw + kOffKs + tok, s_tab, k8, tok, hh, live);
     fence_proxy_async_smem();
@@ -250,17 +244,12 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_attn_tc_kernel(AttnParams 
       for (int k = 0; k < 4; ++k) umma_e4m3(tmem, adesc + 2 * k, bdesc + 2 * k, idesc_qk, k > 0);
       umma_commit(bar_qk);
     }
-    if (e > 0) fold_o();
+    if (e > 0) fold_o();  // the previous page's PV finished before the barrier above
     // ---- V -> FP8 tile (overlaps the QK MMA; the previous PV is done) ----------------
     dequant_half_row(raw + kOffVc + tok * 64, raw + kOffVs + tok, s_tab, v8, tok, hh, live);
     fence_proxy_async_smem();
-    if (tid == 0) mbar_wait(bar_qk, e & 1, s_abort);
-    tc_fence_before();
-    __syncthreads();
-    if (*s_abort) break;
+    mbar_wait(bar_qk, e & 1, s_abort);
     tc_fence_after();
-    // raw buffer e&1 is consumed by every thread: refill it with page e+2
-    if (tid == 0 && e + 2 < n_pg) issue_raw(e + 2);
     // ---- softmax over this page -----------------------------------------------------
     float sv[4];
     tmem_ld4(tmem + ((uint32_t)(32 * quad) << 16), sv);
@@ -268,10 +257,12 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_attn_tc_kernel(AttnParams 
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       x[h] = live ? sv[h] * p.scale_log2 : -INFINITY;
-      const float wm = ord2f(__reduce_max_sync(0xffffffffu, f2ord(x[h])));
+      const float wm = warp_max(x[h]);
       if (lane == 0) s_red[warp * 4 + h] = wm;
     }
-    __syncthreads();
+    __syncthreads();  // page maxima complete; raw buffer e&1 no longer read
+    if (*s_abort) break;
+    if (tid == 0 && e + 2 < n_pg) issue_raw(e + 2);
     uint32_t p_hi = 0, p_lo = 0;
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
@@ -279,9 +270,9 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_attn_tc_kernel(AttnParams 
       const float mp = fmaxf(fmaxf(s_red[h], s_red[4 + h]), fmaxf(s_red[8 + h], s_red[12 + h]));
       const float m_new = fmaxf(m_run[h], mp);
       // m_new = -inf only while no key so far is visible (then everything is 0)
-      alpha_prev[h] = m_new == -INFINITY ? 1.f : exp2f(m_run[h] - m_new);
-      beta_prev[h] = mp == -INFINITY ? 0.f : exp2f(mp - m_new);  // page scale -> running scale
-      const float pr = mp == -INFINITY ? 0.f : exp2f(x[h] - mp);  // relative to the page max
+      alpha_prev[h] = m_new == -INFINITY ? 1.f : fast_exp2(m_run[h] - m_new);
+      beta_prev[h] = mp == -INFINITY ? 0.f : fast_exp2(mp - m_new);  // page scale -> running scale
+      const float pr = mp == -INFINITY ? 0.f : fast_exp2(x[h] - mp);  // relative to the page max
       l_run[h] = l_run[h] * alpha_prev[h] + (hh == 0 ? pr * beta_prev[h] : 0.f);  // this token
       m_run[h] = m_new;
       const float v256 = pr * 256.f;

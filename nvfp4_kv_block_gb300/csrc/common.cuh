@@ -87,6 +87,19 @@ __device__ __forceinline__ uint32_t ordered_bits(float f) {
   uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+__device__ __forceinline__ float from_ordered_bits(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+// Warp-wide max of a float with one redux.sync on its order-preserving bits.
+__device__ __forceinline__ float warp_max(float x) {
+  return from_ordered_bits(__reduce_max_sync(0xffffffffu, ordered_bits(x)));
+}
+// 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // ---- NVFP4 -> FP8 dequantisation --------------------------------------------
 // Table entry for scale byte sb: 8 E4M3 bytes, entry m = E4M3_RNE(|e2m1(m)| * sb),

@@ -307,9 +307,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
 #pragma unroll
         for (int jj = 0; jj < kNqMax; ++jj) {
           if (jj < nq) {
-            float x = m[jj];
-#pragma unroll
-            for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+            const float x = warp_max(m[jj]);
             if (lane == jj) mine = x;
           }
         }
@@ -335,13 +333,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
 
 // ---------------------------------------------------------------------------
 // Top-16 + recent per query token.  Keys are (ordered score << 32) | ~block,
-// unique, larger = better (higher score, then lower block).  256 threads in 16
-// half-warps; half-warp h owns the blocks with (block & 15) == h.  The
-// smallest of the 16 half-warp maxima, theta, is the smallest of 16 distinct
-// keys, hence <= the 16th largest key: every winner has key >= theta.  The few
-// candidates >= theta are ranked exactly by counting.
-constexpr int kTopkThreads = 256;
+// unique, larger = better (higher score, then lower block).  512 threads; the
+// block scores are staged in shared memory by one coalesced pass; thread t
+// owns blocks t, t + 512, ...  When every one of the 16 warps owns a block
+// (r > 480), the smallest of the 16 warp maxima, theta, is the smallest of 16
+// distinct keys and hence <= the 16th largest key: every winner has
+// key >= theta; otherwise theta = 0.  The few candidates >= theta are ranked
+// exactly by counting.
+constexpr int kTopkThreads = 512;
 constexpr int kMaxCand = 2048;
+constexpr int kTopkStage = 16384;  // block scores staged in shared memory up to this many blocks
 
 struct TopkParams {
   const float* scores;
@@ -355,31 +356,37 @@ struct TopkParams {
   int* status;
 };
 
-// Block score = max of the four partial maxima the scan wrote for block blk.
-__device__ __forceinline__ unsigned long long block_key(const float* row, int blk) {
-  const float4 q = reinterpret_cast<const float4*>(row)[blk];
-  const float sc = fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w));
-  return ((unsigned long long)ordered_bits(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
-}
-
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
   return a > b ? a : b;
 }
+// Warp-wide max of a 64-bit key with two redux.sync (high word, then low word).
+__device__ __forceinline__ unsigned long long warp_max64(unsigned long long k) {
+  const uint32_t hi = (uint32_t)(k >> 32);
+  const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+  const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? (uint32_t)k : 0u);
+  return ((unsigned long long)mhi << 32) | mlo;
+}
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
-  __shared__ int s_qsl[kMaxSeqs + 1];
-  __shared__ unsigned long long s_hmax[16];
+  extern __shared__ float s_sc[];  // block scores of this token, staged (r <= kTopkStage)
+  __shared__ unsigned long long s_wmax[kTopkThreads / 32];
   __shared__ unsigned long long s_cand[kMaxCand];
-  __shared__ unsigned long long s_red[kTopkThreads / 32];
   __shared__ int s_win[kTopK];
-  __shared__ int s_ncand;
+  __shared__ int s_ncand, s_seq;
   const int j = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i <= p.n_seqs; i += kTopkThreads) s_qsl[i] = p.q_start_loc[i];
+  if (tid == 0) s_seq = -1;
   __syncthreads();
-  const int b = find_seq(s_qsl, p.n_seqs, j);
-  const SeqInfo s = load_seq(b, p.seq_lens, s_qsl, p.max_pages, p.n_q_total);
+  // sequence of token j: the b with q_start_loc[b] <= j < q_start_loc[b+1]
+  for (int base = 0; base < p.n_seqs; base += kTopkThreads) {
+    const int b = base + tid;
+    if (b < p.n_seqs && p.q_start_loc[b] <= j && j < p.q_start_loc[b + 1]) s_seq = b;
+  }
+  __syncthreads();
+  const int b = s_seq;
+  SeqInfo s{0, 0, 0, false};
+  if (b >= 0) s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
   int* out = p.sel + (size_t)j * kSelStride;
-  if (!s.ok || j < s.q0 || j >= s.q0 + s.n_q) {
+  if (b < 0 || !s.ok) {
     pdl_wait();
     pdl_trigger();
     if (tid == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
@@ -389,30 +396,48 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
   }
   const int pos = s.seq_len - s.n_q + (j - s.q0);
   const int r = pos / kPageTokens;
-  const float* row = p.scores + (size_t)j * p.max_pages * 4;
-  pdl_wait();     // block scores come from the scan kernel
+  const float4* row = reinterpret_cast<const float4*>(p.scores + (size_t)j * p.max_pages * 4);
+  pdl_wait();  // block scores come from the scan kernel
   if (r <= kTopK) {
     pdl_trigger();
     if (tid < kSelStride) out[tid] = tid <= r ? tid : -1;
     if (tid == 0) p.n_sel[j] = r + 1;
     return;
   }
-  // thread t owns blocks base, base + 256, ... with base & 15 == t / 16
-  const int base = ((tid & 15) << 4) | (tid >> 4);
-  unsigned long long mykey = 0;
-#pragma unroll 4
-  for (int blk = base; blk < r; blk += kTopkThreads) mykey = umax64(mykey, block_key(row, blk));
-#pragma unroll
-  for (int o = 8; o; o >>= 1) mykey = umax64(mykey, __shfl_xor_sync(0xffffffffu, mykey, o));
-  if ((lane & 15) == 0) s_hmax[tid >> 4] = mykey;
+  // block score = max of the scan's four partial maxima; staged with one
+  // coalesced pass (all loads of a thread in flight together)
+  const bool staged = r <= kTopkStage;
+  auto score = [&](int blk) -> float {
+    if (staged) return s_sc[blk];
+    const float4 v = row[blk];
+    return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+  };
+  auto key = [&](int blk) -> unsigned long long {
+    return ((unsigned long long)ordered_bits(score(blk)) << 32) |
+           (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
+  };
+  if (staged) {
+#pragma unroll 8
+    for (int blk = tid; blk < r; blk += kTopkThreads) {
+      const float4 v = row[blk];
+      s_sc[blk] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    }
+  }
   if (tid == 0) s_ncand = 0;
   __syncthreads();
-  unsigned long long theta = s_hmax[0];
+  unsigned long long theta = 0;
+  if (r > kTopkThreads - 32) {  // every warp owns at least one block
+    unsigned long long mykey = 0;
+    for (int blk = tid; blk < r; blk += kTopkThreads) mykey = umax64(mykey, key(blk));
+    mykey = warp_max64(mykey);
+    if (lane == 0) s_wmax[warp] = mykey;
+    __syncthreads();
+    theta = s_wmax[0];
 #pragma unroll
-  for (int i = 1; i < 16; ++i) theta = s_hmax[i] < theta ? s_hmax[i] : theta;
-#pragma unroll 4
-  for (int blk = base; blk < r; blk += kTopkThreads) {
-    const unsigned long long k = block_key(row, blk);
+    for (int i = 1; i < kTopkThreads / 32; ++i) theta = s_wmax[i] < theta ? s_wmax[i] : theta;
+  }
+  for (int blk = tid; blk < r; blk += kTopkThreads) {
+    const unsigned long long k = key(blk);
     if (k >= theta) {
       const int slot = atomicAdd(&s_ncand, 1);
       if (slot < kMaxCand) s_cand[slot] = k;
@@ -434,16 +459,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
     for (int k = 0; k < kTopK; ++k) {
       unsigned long long best = 0;
       for (int blk = tid; blk < r; blk += kTopkThreads) {
-        const unsigned long long key = block_key(row, blk);
-        if (key < bound) best = umax64(best, key);
+        const unsigned long long kk = key(blk);
+        if (kk < bound) best = umax64(best, kk);
       }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
-      if (lane == 0) s_red[warp] = best;
+      best = warp_max64(best);
+      if (lane == 0) s_wmax[warp] = best;
       __syncthreads();
-      best = s_red[0];
+      best = s_wmax[0];
 #pragma unroll
-      for (int i = 1; i < kTopkThreads / 32; ++i) best = umax64(best, s_red[i]);
+      for (int i = 1; i < kTopkThreads / 32; ++i) best = umax64(best, s_wmax[i]);
       if (tid == 0) s_win[k] = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
       bound = best;
       __syncthreads();
@@ -487,6 +511,9 @@ cudaError_t launch_indexer_topk(const msa_cache* c, const uint8_t* q_idx, const 
     e = cudaFuncSetAttribute(indexer_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)scan_smem_bytes(kMaxSeqs));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kTopkStage * sizeof(float)));
+    if (e != cudaSuccess) return e;
     s_n_sm[dev] = n_sm;
   }
   const int n_sm = s_n_sm[dev];
@@ -494,7 +521,8 @@ cudaError_t launch_indexer_topk(const msa_cache* c, const uint8_t* q_idx, const 
   e = launch_pdl(indexer_scan_kernel, dim3(n_sm), dim3(kScanThreads), smem, stream, sp);
   if (e != cudaSuccess) return e;
   TopkParams tp{scores, max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, sel, n_sel, c->status};
-  return launch_pdl(topk_kernel, dim3(n_q_total), dim3(kTopkThreads), 0, stream, tp);
+  const size_t topk_smem = (size_t)min(max_pages, kTopkStage) * sizeof(float);
+  return launch_pdl(topk_kernel, dim3(n_q_total), dim3(kTopkThreads), topk_smem, stream, tp);
 }
 
 }  // namespace msa
