@@ -1,8 +1,8 @@
 """Benchmark of the NVFP4 block-sparse attention decode step on GB300.
 
-One step = indexer scan + top-16/recent selection + split sparse attention +
-LSE merge (the decode path's four kernels) over one batch of resident query
-tokens.  Prints ONE JSON line (rank 0).
+One step = indexer (block scores + top-16/recent selection, one cooperative
+launch) + split sparse attention + LSE merge (the decode path's three kernels)
+over one batch of resident query tokens.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl gb300|reference]
 
@@ -247,7 +247,7 @@ def run_gpu(args, rank, world, local_rank):
         ms, t_idx, e2e = (float(x) for x in t.cpu())
     return dict(wl=wl, T=T, ms=ms, t_idx=t_idx, e2e=e2e, h2d=h2d, d2h=d2h, n_splits=n_splits,
                 idx_bytes=idx_bytes, kv_bytes=kv_bytes, alg_bytes=alg_bytes, clocks=clk,
-                launches=4 * args.steps)
+                launches=3 * args.steps)
 
 
 def oracle_sample(wl, device, budget_s):
@@ -365,7 +365,7 @@ def main():
                 "kv_bytes": r["kv_bytes"], "achieved_gbs": step_gbs,
                 "frac_of_8tbs": step_gbs / ROOFLINE_NOMINAL_GBS,
                 f"frac_of_{peak_kind}": step_gbs / peak},
-        "roofline": {"kernel": "indexer (scan + top-k launches of msa_indexer_topk)", "bound": "hbm",
+        "roofline": {"kernel": "indexer_scan_kernel (msa_indexer_topk: block scores + selection)", "bound": "hbm",
                      "achieved": idx_gbs, "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak,
                      "peak_kind": peak_kind, "traffic": committed_traffic(wl.name),
                      "algorithmic_bytes_per_launch": r["idx_bytes"], "ms_per_launch": r["t_idx"]},

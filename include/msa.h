@@ -133,12 +133,16 @@ int msa_quantize_kv_insert(const msa_cache* cache, const float* k, const float* 
  *               ids of blocks 0..r_j-1 (highest block score first wins, ties to
  *               the lower id) in ascending order, then r_j; padded with -1.
  *   n_sel       int32 [n_q_total] out: min(topk, r_j) + 1.
- *   ws, ws_bytes scratch of at least msa_indexer_workspace_bytes(...) bytes.
- *               After the stream reaches the end of this call it holds, for
- *               every query token j and block i < r_j, four fp32 partial maxima
- *               P[j][i][0..3] (row stride 4 * max_pages floats): the maxima over
- *               the block's token quarters; the block score is their max.  Other
- *               entries are unspecified.
+ *   ws, ws_bytes scratch of at least msa_indexer_workspace_bytes(...) bytes,
+ *               16-byte aligned, ZEROED before its first use (every call leaves
+ *               its first 256 bytes -- grid-barrier words -- as it found them
+ *               up to a generation count, so later calls need no clearing).  From
+ *               byte 256, after the stream reaches the end of this call, it holds
+ *               for every query token j and block i < r_j four fp32 partial
+ *               maxima P[j][i][0..3] (row stride 4 * max_pages floats): the maxima
+ *               over the block's token quarters; the block score is their max.
+ *               Other entries are unspecified.  Calls sharing a workspace must
+ *               not overlap on the GPU.
  * Block score S[j][i] = max over the 128 tokens t of block i of
  *   sum_h w[j][h] * max(0, q_idx[j][h] . key(t)), computed with fp32 sums of
  *   exact FP8 products.
@@ -167,13 +171,15 @@ size_t msa_indexer_workspace_bytes(int32_t n_q_total, int32_t max_pages);
  * the process exits.  Shapes that need more, i.e.
  * msa_indexer_workspace_bytes(n_q_total, max_pages) > that capacity, return
  * MSA_ERR_SCRATCH_CAPACITY and enqueue nothing.  Nothing in the array needs
- * clearing: every entry a call reads was written earlier by that same call.
+ * clearing by the caller: every score entry a call reads was written earlier
+ * by that same call.
  * The array is shared by all calls on a device and keeps the last call's
  * contents, so calls whose kernels overlap on the GPU (e.g. on two streams
  * without ordering) race and must not be issued.  The first call on each
  * device looks up the array's device address (with that device current);
  * make that first call before any stream capture.  No cudaMalloc, cudaFree
- * or allocating routine is called.
+ * or allocating routine is called.  (The array starts zeroed when the library
+ * is loaded; its grid-barrier words return to rest after every call.)
  */
 int msa_indexer_topk_noalloc(const msa_cache* cache, const uint8_t* q_idx, const float* w,
                              int32_t n_idx_heads, const int32_t* block_table, int32_t max_pages,

@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_attn_tc_kernel(AttnParams 
     *reinterpret_cast<uint4*>(qp + row * 128 + ((c ^ row) << 4)) = v;
   }
 
-  pdl_wait();  // the selection comes from the top-k kernel
+  pdl_wait();  // the selection comes from the indexer kernel
   const int nsel = seq_ok ? min(p.n_sel[j], kSelStride) : 0;
   if (tid < kSelStride) {
     const int e = split + tid * p.n_splits;

@@ -134,16 +134,6 @@ __device__ __forceinline__ uint2 dequant8(uint32_t w, uint2 t) {
   return make_uint2(mag0 | (s0 & 0x80808080u), mag1 | (s1 & 0x80808080u));
 }
 
-// ---- tensor cores: mma.sync m16n8k32, E4M3 x E4M3 -> fp32 --------------------
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-
 // ---- mbarrier / TMA bulk copy / tcgen05 (inline PTX) --------------------------
 // Every wait is bounded: after kSpinLimit polls the caller gets false and must
 // abandon its loop (the kernel then reports MSA_STATUS_TIMEOUT).

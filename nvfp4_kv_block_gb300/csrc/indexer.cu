@@ -43,6 +43,9 @@ struct ScanParams {
   int n_seqs;
   int n_q_total;
   float* scores;  // [T][max_pages][4] partial block maxima
+  int* sel;       // [T][17]
+  int* n_sel;     // [T]
+  unsigned int* sync;  // grid barrier words: [0] arrivals, [1] generation
   int* status;
 };
 
@@ -91,6 +94,176 @@ __device__ __forceinline__ void for_each_segment(const ScanParams& p, const int*
   }
 }
 
+// ---------------------------------------------------------------------------
+// Top-16 + recent per query token, run by the scan kernel's CTAs after a grid
+// barrier (every block score is then written).  Keys are
+// (ordered score << 32) | ~block: unique, larger = better (higher score, then
+// lower block).  The token's block scores are staged in shared memory by one
+// coalesced pass, a lower bound theta of the 16th largest key prunes them to a
+// few candidates, which are ranked exactly by counting.
+constexpr int kMaxCand = 2048;
+constexpr int kTopkStage = 16384;  // block scores staged in shared memory up to this many blocks
+constexpr int kWsSyncBytes = 256;  // grid-barrier words at the start of the indexer workspace
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
+struct TopkSmem {
+  float* sc;                 // [kTopkStage]
+  unsigned long long* cand;  // [kMaxCand]
+  unsigned long long* tmax;  // [NT] half-warp maxima / reduction scratch
+  int* win;                  // [16]
+  int* misc;                 // [0] n_cand, [1] sequence
+};
+
+// Sequence of query token j (-1 if none): the b with q_start_loc[b] <= j <
+// q_start_loc[b+1], found by all NT threads in one pass.
+template <int NT>
+__device__ int token_sequence(const ScanParams& p, int j, int* slot) {
+  if (threadIdx.x == 0) *slot = -1;
+  __syncthreads();
+  for (int base = 0; base < p.n_seqs; base += NT) {
+    const int b = base + threadIdx.x;
+    if (b < p.n_seqs && p.q_start_loc[b] <= j && j < p.q_start_loc[b + 1]) *slot = b;
+  }
+  __syncthreads();
+  return *slot;
+}
+
+template <int NT>
+__device__ void select_token(const ScanParams& p, int j, int b, const TopkSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  SeqInfo s{0, 0, 0, false};
+  if (b >= 0) s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
+  int* out = p.sel + (size_t)j * kSelStride;
+  if (b < 0 || !s.ok) {
+    if (tid == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
+    if (tid < kSelStride) out[tid] = -1;
+    if (tid == 0) p.n_sel[j] = 0;
+    return;
+  }
+  const int pos = s.seq_len - s.n_q + (j - s.q0);
+  const int r = pos / kPageTokens;
+  if (r <= kTopK) {
+    if (tid < kSelStride) out[tid] = tid <= r ? tid : -1;
+    if (tid == 0) p.n_sel[j] = r + 1;
+    return;
+  }
+  // block score = max of the four partial maxima (written by other CTAs: read
+  // through L2)
+  const float4* row = reinterpret_cast<const float4*>(p.scores + (size_t)j * p.max_pages * 4);
+  const bool staged = r <= kTopkStage;
+  auto score = [&](int blk) -> float {
+    if (staged) return sm.sc[blk];
+    const float4 v = __ldcg(row + blk);
+    return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+  };
+  auto key = [&](int blk) -> unsigned long long {
+    return ((unsigned long long)ordered_bits(score(blk)) << 32) |
+           (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
+  };
+  if (staged) {
+#pragma unroll 8
+    for (int blk = tid; blk < r; blk += NT) {
+      const float4 v = __ldcg(row + blk);
+      sm.sc[blk] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    }
+  }
+  if (tid == 0) sm.misc[0] = 0;
+  __syncthreads();
+  // theta: thread t owns blocks t, t + NT, ...; half-warp h owns the blocks with
+  // (blk mod NT) in [16h, 16h+16).  When all NT/16 >= 16 half-warps own a block
+  // (r > NT - 16), their maxima are NT/16 distinct keys whose minimum is <= the
+  // 16th largest key; otherwise theta = 0 and every block is a candidate.
+  unsigned long long theta = 0;
+  if (r > NT - 16) {
+    unsigned long long mykey = 0;
+    for (int blk = tid; blk < r; blk += NT) mykey = umax64(mykey, key(blk));
+#pragma unroll
+    for (int o = 8; o; o >>= 1) mykey = umax64(mykey, __shfl_xor_sync(0xffffffffu, mykey, o));
+    if ((lane & 15) == 0) sm.tmax[tid >> 4] = mykey;
+    __syncthreads();
+    theta = sm.tmax[0];
+#pragma unroll 4
+    for (int i = 1; i < NT / 16; ++i) theta = sm.tmax[i] < theta ? sm.tmax[i] : theta;
+  }
+  for (int blk = tid; blk < r; blk += NT) {
+    const unsigned long long k = key(blk);
+    if (k >= theta) {
+      const int slot = atomicAdd(&sm.misc[0], 1);
+      if (slot < kMaxCand) sm.cand[slot] = k;
+    }
+  }
+  __syncthreads();
+  const int nc = sm.misc[0];
+  if (nc <= kMaxCand) {
+    for (int c = tid; c < nc; c += NT) {
+      const unsigned long long k = sm.cand[c];
+      int rk = 0;
+      for (int i = 0; i < nc; ++i) rk += sm.cand[i] > k;
+      if (rk < kTopK) sm.win[rk] = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFu));
+    }
+  } else {
+    // too many candidates for the buffer (adversarial score layouts): 16 rounds
+    // of CTA-wide argmax, each over the keys below the previous winner
+    unsigned long long bound = ~0ull;
+    for (int k = 0; k < kTopK; ++k) {
+      unsigned long long best = 0;
+      for (int blk = tid; blk < r; blk += NT) {
+        const unsigned long long kk = key(blk);
+        if (kk < bound) best = umax64(best, kk);
+      }
+      sm.tmax[tid] = best;
+      __syncthreads();
+      if (tid == 0) {
+        for (int i = 1; i < NT; ++i) best = umax64(best, sm.tmax[i]);
+        sm.tmax[0] = best;
+        sm.win[k] = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+      }
+      __syncthreads();
+      bound = sm.tmax[0];
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  if (tid < kTopK) {
+    const int blk = sm.win[tid];
+    int at = 0;
+#pragma unroll
+    for (int i = 0; i < kTopK; ++i) at += sm.win[i] < blk;
+    out[at] = blk;
+  }
+  if (tid == 0) {
+    out[kTopK] = r;
+    p.n_sel[j] = kTopK + 1;
+  }
+}
+
+// Grid-wide barrier of a cooperative launch (all CTAs co-resident): arrival
+// counter back to zero at every release, generation word bumped.  Bounded: on
+// timeout it raises *abort and returns false.
+__device__ bool grid_barrier(unsigned int* sync, unsigned int n_ctas, volatile int* abort) {
+  __threadfence();
+  volatile unsigned int* gen = sync + 1;
+  const unsigned int g = *gen;
+  if (atomicAdd(sync, 1u) == n_ctas - 1) {
+    atomicExch(sync, 0u);
+    __threadfence();
+    atomicAdd(sync + 1, 1u);
+    return true;
+  }
+  for (uint32_t i = 0; i < (kSpinLimit >> 4); ++i) {
+    if (*gen != g) {
+      __threadfence();
+      return true;
+    }
+    __nanosleep(64);
+  }
+  *abort = 1;
+  return false;
+}
+
 __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -110,7 +283,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();     // inputs may come from the previous kernel in the stream
-  pdl_trigger();  // the top-k kernel may launch and run its prologue
+  pdl_trigger();  // the attention kernel may launch and run its prologue
 
   // -- exclusive prefix over sequences of the pages each one scans ------------
   {
@@ -261,7 +434,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   } else {
     // ---------------- epilogue: two sets of four warps, set = page parity ------
     // warps 2..5 and 6..9 -> TMEM lane quadrants 2,3,0,1; each warp writes the
-    // max over its 32 token rows, the top-k kernel takes the max of the four.
+    // max over its 32 token rows, the top-k phase takes the max of the four.
     const int quad = warp & 3, set = (warp - 2) >> 2;
     int it = 0;
     for_each_segment(p, s_prefix, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
@@ -321,171 +494,33 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
     });
   }
 
-  // ---------------- teardown -------------------------------------------------
+  // ---------------- scan teardown ---------------------------------------------
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+
+  // ---------------- every block score written: top-k, tokens spread over CTAs --
+  TopkSmem sm;
+  sm.sc = reinterpret_cast<float*>(smem + kOffStages);                                 // 64 KB
+  sm.cand = reinterpret_cast<unsigned long long*>(smem + kOffStages + 4 * kTopkStage);  // 16 KB
+  sm.tmax = reinterpret_cast<unsigned long long*>(smem + kOffB);                       // NT x 8 B
+  sm.win = reinterpret_cast<int*>(smem + kOffB + 8 * kScanThreads);
+  sm.misc = sm.win + kTopK;
+  // the first token's sequence is looked up while other CTAs finish scanning
+  int b_first = blockIdx.x < p.n_q_total ? token_sequence<kScanThreads>(p, blockIdx.x, sm.misc + 1) : -1;
+  if (tid == 0 && !*s_abort) grid_barrier(p.sync, gridDim.x, s_abort);
+  __syncthreads();
+  if (!*s_abort) {
+    for (int j = blockIdx.x; j < p.n_q_total; j += gridDim.x) {
+      const int b = j == (int)blockIdx.x ? b_first : token_sequence<kScanThreads>(p, j, sm.misc + 1);
+      select_token<kScanThreads>(p, j, b, sm);
+      __syncthreads();
+    }
+  }
   if (tid == 0 && *s_abort) set_status(p.status, MSA_STATUS_TIMEOUT);
-}
-
-// ---------------------------------------------------------------------------
-// Top-16 + recent per query token.  Keys are (ordered score << 32) | ~block,
-// unique, larger = better (higher score, then lower block).  512 threads; the
-// block scores are staged in shared memory by one coalesced pass; thread t
-// owns blocks t, t + 512, ...  When every one of the 16 warps owns a block
-// (r > 480), the smallest of the 16 warp maxima, theta, is the smallest of 16
-// distinct keys and hence <= the 16th largest key: every winner has
-// key >= theta; otherwise theta = 0.  The few candidates >= theta are ranked
-// exactly by counting.
-constexpr int kTopkThreads = 512;
-constexpr int kMaxCand = 2048;
-constexpr int kTopkStage = 16384;  // block scores staged in shared memory up to this many blocks
-
-struct TopkParams {
-  const float* scores;
-  int max_pages;
-  const int* seq_lens;
-  const int* q_start_loc;
-  int n_seqs;
-  int n_q_total;
-  int* sel;
-  int* n_sel;
-  int* status;
-};
-
-__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
-  return a > b ? a : b;
-}
-// Warp-wide max of a 64-bit key with two redux.sync (high word, then low word).
-__device__ __forceinline__ unsigned long long warp_max64(unsigned long long k) {
-  const uint32_t hi = (uint32_t)(k >> 32);
-  const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
-  const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? (uint32_t)k : 0u);
-  return ((unsigned long long)mhi << 32) | mlo;
-}
-
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
-  extern __shared__ float s_sc[];  // block scores of this token, staged (r <= kTopkStage)
-  __shared__ unsigned long long s_wmax[kTopkThreads / 32];
-  __shared__ unsigned long long s_cand[kMaxCand];
-  __shared__ int s_win[kTopK];
-  __shared__ int s_ncand, s_seq;
-  const int j = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) s_seq = -1;
-  __syncthreads();
-  // sequence of token j: the b with q_start_loc[b] <= j < q_start_loc[b+1]
-  for (int base = 0; base < p.n_seqs; base += kTopkThreads) {
-    const int b = base + tid;
-    if (b < p.n_seqs && p.q_start_loc[b] <= j && j < p.q_start_loc[b + 1]) s_seq = b;
-  }
-  __syncthreads();
-  const int b = s_seq;
-  SeqInfo s{0, 0, 0, false};
-  if (b >= 0) s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
-  int* out = p.sel + (size_t)j * kSelStride;
-  if (b < 0 || !s.ok) {
-    pdl_wait();
-    pdl_trigger();
-    if (tid == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
-    if (tid < kSelStride) out[tid] = -1;
-    if (tid == 0) p.n_sel[j] = 0;
-    return;
-  }
-  const int pos = s.seq_len - s.n_q + (j - s.q0);
-  const int r = pos / kPageTokens;
-  const float4* row = reinterpret_cast<const float4*>(p.scores + (size_t)j * p.max_pages * 4);
-  pdl_wait();  // block scores come from the scan kernel
-  if (r <= kTopK) {
-    pdl_trigger();
-    if (tid < kSelStride) out[tid] = tid <= r ? tid : -1;
-    if (tid == 0) p.n_sel[j] = r + 1;
-    return;
-  }
-  // block score = max of the scan's four partial maxima; staged with one
-  // coalesced pass (all loads of a thread in flight together)
-  const bool staged = r <= kTopkStage;
-  auto score = [&](int blk) -> float {
-    if (staged) return s_sc[blk];
-    const float4 v = row[blk];
-    return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-  };
-  auto key = [&](int blk) -> unsigned long long {
-    return ((unsigned long long)ordered_bits(score(blk)) << 32) |
-           (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
-  };
-  if (staged) {
-#pragma unroll 8
-    for (int blk = tid; blk < r; blk += kTopkThreads) {
-      const float4 v = row[blk];
-      s_sc[blk] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-    }
-  }
-  if (tid == 0) s_ncand = 0;
-  __syncthreads();
-  unsigned long long theta = 0;
-  if (r > kTopkThreads - 32) {  // every warp owns at least one block
-    unsigned long long mykey = 0;
-    for (int blk = tid; blk < r; blk += kTopkThreads) mykey = umax64(mykey, key(blk));
-    mykey = warp_max64(mykey);
-    if (lane == 0) s_wmax[warp] = mykey;
-    __syncthreads();
-    theta = s_wmax[0];
-#pragma unroll
-    for (int i = 1; i < kTopkThreads / 32; ++i) theta = s_wmax[i] < theta ? s_wmax[i] : theta;
-  }
-  for (int blk = tid; blk < r; blk += kTopkThreads) {
-    const unsigned long long k = key(blk);
-    if (k >= theta) {
-      const int slot = atomicAdd(&s_ncand, 1);
-      if (slot < kMaxCand) s_cand[slot] = k;
-    }
-  }
-  __syncthreads();
-  const int nc = s_ncand;
-  if (nc <= kMaxCand) {
-    for (int c = tid; c < nc; c += kTopkThreads) {
-      const unsigned long long k = s_cand[c];
-      int rk = 0;
-      for (int i = 0; i < nc; ++i) rk += s_cand[i] > k;
-      if (rk < kTopK) s_win[rk] = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFu));
-    }
-  } else {
-    // too many candidates for the buffer (adversarial score layouts): 16 rounds
-    // of block-wide argmax, each over the keys below the previous winner
-    unsigned long long bound = ~0ull;
-    for (int k = 0; k < kTopK; ++k) {
-      unsigned long long best = 0;
-      for (int blk = tid; blk < r; blk += kTopkThreads) {
-        const unsigned long long kk = key(blk);
-        if (kk < bound) best = umax64(best, kk);
-      }
-      best = warp_max64(best);
-      if (lane == 0) s_wmax[warp] = best;
-      __syncthreads();
-      best = s_wmax[0];
-#pragma unroll
-      for (int i = 1; i < kTopkThreads / 32; ++i) best = umax64(best, s_wmax[i]);
-      if (tid == 0) s_win[k] = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
-      bound = best;
-      __syncthreads();
-    }
-  }
-  __syncthreads();
-  if (tid < kTopK) {
-    const int blk = s_win[tid];
-    int at = 0;
-#pragma unroll
-    for (int i = 0; i < kTopK; ++i) at += s_win[i] < blk;
-    out[at] = blk;
-  }
-  if (tid == 0) {
-    out[kTopK] = r;
-    p.n_sel[j] = kTopK + 1;
-  }
-  pdl_trigger();  // the attention kernel may launch now (it waits for this grid to finish)
 }
 
 }  // namespace
@@ -493,10 +528,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
 cudaError_t launch_indexer_topk(const msa_cache* c, const uint8_t* q_idx, const float* w,
                                 const int* block_table, int max_pages, const int* seq_lens,
                                 const int* q_start_loc, int n_seqs, int n_q_total, int* sel,
-                                int* n_sel, float* scores, cudaStream_t stream) {
+                                int* n_sel, void* ws, cudaStream_t stream) {
   if (n_q_total == 0 || n_seqs == 0) return cudaSuccess;
+  // workspace: [0, 256) grid-barrier words, then the partial block maxima
+  unsigned int* sync = static_cast<unsigned int*>(ws);
+  float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsSyncBytes);
   ScanParams sp{static_cast<const uint8_t*>(c->idx_pool), c->n_pages, q_idx, w, block_table,
-                max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, scores, c->status};
+                max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, scores, sel, n_sel, sync,
+                c->status};
   // per-device launch set-up, done once (not a stream operation, so a later call
   // may be captured into a CUDA graph)
   static int s_n_sm[64] = {0};
@@ -511,18 +550,21 @@ cudaError_t launch_indexer_topk(const msa_cache* c, const uint8_t* q_idx, const 
     e = cudaFuncSetAttribute(indexer_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)scan_smem_bytes(kMaxSeqs));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kTopkStage * sizeof(float)));
-    if (e != cudaSuccess) return e;
     s_n_sm[dev] = n_sm;
   }
-  const int n_sm = s_n_sm[dev];
-  const size_t smem = scan_smem_bytes(n_seqs);
-  e = launch_pdl(indexer_scan_kernel, dim3(n_sm), dim3(kScanThreads), smem, stream, sp);
-  if (e != cudaSuccess) return e;
-  TopkParams tp{scores, max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, sel, n_sel, c->status};
-  const size_t topk_smem = (size_t)min(max_pages, kTopkStage) * sizeof(float);
-  return launch_pdl(topk_kernel, dim3(n_q_total), dim3(kTopkThreads), topk_smem, stream, tp);
+  // one CTA per SM, all co-resident (cooperative launch): the top-k phase
+  // waits for every CTA's scan at a grid barrier
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s_n_sm[dev]);
+  cfg.blockDim = dim3(kScanThreads);
+  cfg.dynamicSmemBytes = scan_smem_bytes(n_seqs);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, indexer_scan_kernel, sp);
 }
 
 }  // namespace msa
@@ -561,7 +603,7 @@ cudaError_t launch_indexer_topk_noalloc(const msa_cache* c, const uint8_t* q_idx
     scratch = g_static_ptr[dev];
   }
   return launch_indexer_topk(c, q_idx, w, block_table, max_pages, seq_lens, q_start_loc, n_seqs,
-                             n_q_total, sel, n_sel, scratch, stream);
+                             n_q_total, sel, n_sel, static_cast<void*>(scratch), stream);
 }
 
 }  // namespace msa

@@ -9,14 +9,10 @@ cudaError_t launch_quantize_insert(const msa_cache*, const float*, const float*,
                                    const int64_t*, int, cudaStream_t);
 cudaError_t launch_absmax(const float*, int64_t, float*, cudaStream_t);
 cudaError_t launch_indexer_topk(const msa_cache*, const uint8_t*, const float*, const int*, int,
-                                const int*, const int*, int, int, int*, int*, float*,
-                                cudaStream_t);
+                                const int*, const int*, int, int, int*, int*, void*, cudaStream_t);
 cudaError_t launch_indexer_topk_noalloc(const msa_cache*, const uint8_t*, const float*, const int*,
                                         int, const int*, const int*, int, int, int*, int*,
                                         cudaStream_t);
-cudaError_t launch_sparse_attn(const msa_cache*, const uint8_t*, float, const int*, const int*,
-                               const int*, int, const int*, const int*, int, int, int, float*,
-                               float*, cudaStream_t);
 cudaError_t launch_sparse_attn_tc(const msa_cache*, const uint8_t*, float, const int*, const int*,
                                   const int*, int, const int*, const int*, int, int, int, float*,
                                   float*, cudaStream_t);
@@ -58,9 +54,10 @@ int msa_quantize_kv_insert(const msa_cache* cache, const float* k, const float* 
 }
 
 size_t msa_indexer_workspace_bytes(int32_t n_q_total, int32_t max_pages) {
+  // 256 bytes of grid-barrier words, then 4 partial maxima per (token, block)
   if (n_q_total <= 0 || max_pages <= 0) return 256;
   const size_t b = (size_t)n_q_total * (size_t)max_pages * 4 * sizeof(float);
-  return (b + 255) / 256 * 256;
+  return 256 + (b + 255) / 256 * 256;
 }
 
 int msa_indexer_topk(const msa_cache* cache, const uint8_t* q_idx, const float* w,
@@ -81,8 +78,7 @@ int msa_indexer_topk(const msa_cache* cache, const uint8_t* q_idx, const float* 
   if (ws_bytes < msa_indexer_workspace_bytes(n_q_total, max_pages))
     return MSA_ERR_WORKSPACE_TOO_SMALL;
   return launched(msa::launch_indexer_topk(cache, q_idx, w, block_table, max_pages, seq_lens,
-                                           q_start_loc, n_seqs, n_q_total, sel, n_sel,
-                                           static_cast<float*>(ws),
+                                           q_start_loc, n_seqs, n_q_total, sel, n_sel, ws,
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -178,8 +178,8 @@ def indexer_topk(cache, q_idx, w, block_table, seq_lens, q_start_loc, ws=None, s
     if tuple(seq_lens.shape) != (n_seqs,) or tuple(q_start_loc.shape) != (n_seqs + 1,):
         raise ValueError("seq_lens must be [B], q_start_loc [B+1]")
     dev = q_idx.device
-    if ws is None:
-        ws = torch.empty(indexer_workspace_bytes(T, max_pages), dtype=torch.uint8, device=dev)
+    if ws is None:  # zeroed: its first bytes are grid-barrier words
+        ws = torch.zeros(indexer_workspace_bytes(T, max_pages), dtype=torch.uint8, device=dev)
     if sel is None:
         sel = torch.empty((T, topk + 1), dtype=torch.int32, device=dev)
     if n_sel is None:
@@ -220,7 +220,7 @@ def indexer_topk_noalloc(cache, q_idx, w, block_table, seq_lens, q_start_loc, se
 def block_scores_view(ws, n_q_total, max_pages):
     """The fp32 block scores S[T, max_pages]: max of the four partial maxima per
     block held in the indexer workspace (valid for blocks < r_j)."""
-    part = ws[: n_q_total * max_pages * 16].view(torch.float32).view(n_q_total, max_pages, 4)
+    part = ws[256: 256 + n_q_total * max_pages * 16].view(torch.float32).view(n_q_total, max_pages, 4)
     return part.amax(dim=-1)
 
 
@@ -290,7 +290,7 @@ class DecodeBuffers:
 
     def __init__(self, n_q_total, max_pages, n_splits, device="cuda"):
         self.T, self.n_splits = n_q_total, n_splits
-        self.ws = torch.empty(indexer_workspace_bytes(n_q_total, max_pages), dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(indexer_workspace_bytes(n_q_total, max_pages), dtype=torch.uint8, device=device)
         self.sel = torch.empty((n_q_total, TOPK + 1), dtype=torch.int32, device=device)
         self.n_sel = torch.empty((n_q_total,), dtype=torch.int32, device=device)
         self.o_part = torch.empty((n_q_total, n_splits, Q_HEADS, HEAD_DIM), dtype=torch.float32, device=device)
@@ -299,7 +299,7 @@ class DecodeBuffers:
 
 
 def decode_step(cache, q, q_idx, w, block_table, seq_lens, q_start_loc, bufs, softmax_scale=None):
-    """One decode step: indexer top-k, sparse attention splits, LSE merge (4 kernels)."""
+    """One decode step: indexer top-k, sparse attention splits, LSE merge (3 kernels)."""
     indexer_topk(cache, q_idx, w, block_table, seq_lens, q_start_loc, ws=bufs.ws, sel=bufs.sel,
                  n_sel=bufs.n_sel)
     sparse_attn_decode(cache, q, bufs.sel, bufs.n_sel, block_table, seq_lens, q_start_loc,

@@ -39,7 +39,7 @@ def test_encode_scale_matches_oracle(lib):
 
 
 def test_workspace_bytes(lib):
-    assert ops.indexer_workspace_bytes(32, 256) == 32 * 256 * 16
+    assert ops.indexer_workspace_bytes(32, 256) == 256 + 32 * 256 * 16
     assert ops.indexer_workspace_bytes(3, 5) % 256 == 0 and ops.indexer_workspace_bytes(3, 5) >= 60
 
 
