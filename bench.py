@@ -44,26 +44,28 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the indexer kernel's sources (its DRAM counters go stale when they change)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_kv_block_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in ("common.cuh", "indexer.cu"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic(config_name):
-    """DRAM bytes per indexer launch from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", "indexer_traffic.json")
+    """DRAM bytes per indexer launch from the committed ncu summary
+    (profiles/indexer_traffic.txt: lines "workload source_hash bytes"), if it
+    was taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "indexer_traffic.txt")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f)
-    e = d.get(config_name)
-    if not e or e.get("source_hash") != kernel_source_hash():
-        return None
-    return e.get("dram_bytes_per_launch")
+        for line in f:
+            parts = line.split()
+            if len(parts) == 3 and not line.startswith("#") and parts[0] == config_name:
+                return float(parts[2]) if parts[1] == kernel_source_hash() else None
+    return None
 
 
 class ClockSampler:
