@@ -36,9 +36,11 @@
  * Page formats (one physical page id p addresses both pools):
  *   KV page p at kv_pool + p * 73,728 bytes = 4 heads x 18,432 bytes; head g
  *   at offset g * 18,432:
- *     +0       K codes  [128 tokens][64 B]: byte i = code(ch 2i) | code(ch 2i+1) << 4
+ *     +0       K codes  [128 tokens][64 B]: byte i = code(ch 2i) | code(ch 2i+1) << 4,
+ *              with the 16-byte chunk c (channels 32c..32c+31) of token t stored
+ *              at chunk position c XOR ((t >> 1) mod 4) of its row
  *     +8,192   K scales [8 groups][128 tokens]: E4M3 scale of channels 16k..16k+15
- *     +9,216   V codes  [128 tokens][64 B]
+ *     +9,216   V codes  [128 tokens][64 B], chunks placed like the K codes
  *     +17,408  V scales [8 groups][128 tokens]
  *   (576 bytes per token and layer: the 34,560 bytes/token of the ai4snews
  *   article over the model's layers.)

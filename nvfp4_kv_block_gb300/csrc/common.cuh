@@ -26,6 +26,11 @@ constexpr int kHeadBytes = 18432;
 constexpr int kKvPageBytes = kKvHeads * kHeadBytes;  // 73,728
 constexpr int kIdxPageBytes = kPageTokens * kIdxDim;  // 16,384
 constexpr int kOffKc = 0, kOffKs = 8192, kOffVc = 9216, kOffVs = 17408;
+// The 16-byte code chunk c (channels 32c..32c+31) of token t sits at chunk
+// position c ^ ((t >> 1) & 3) of the token's 64-byte code row: one thread per
+// token can then read chunk c of 32 consecutive rows (64 B apart) without
+// shared-memory bank conflicts.
+__host__ __device__ __forceinline__ int code_chunk_pos(int c, int t) { return c ^ ((t >> 1) & 3); }
 constexpr int kMaxSeqs = 4096;
 constexpr int kMaxSplits = 64;
 // Capacity of the file-scope scratch of msa_indexer_topk_noalloc.

@@ -47,7 +47,9 @@ __global__ void __launch_bounds__(256) debug_fp8_page_kernel(const uint8_t* __re
   if (id >= 2 * kKvHeads * kPageTokens * 8) return;
   const int grp = id & 7, tok = (id >> 3) & 127, head = (id >> 10) & 3, isv = id >> 12;
   const uint8_t* base = kv_pool + (size_t)page * kKvPageBytes + head * kHeadBytes;
-  const uint8_t* codes = base + (isv ? kOffVc : kOffKc) + tok * 64 + grp * 8;
+  // group grp = 8 code bytes at offset 8 (grp & 1) of code chunk grp >> 1
+  const uint8_t* codes = base + (isv ? kOffVc : kOffKc) + tok * 64 +
+                         (code_chunk_pos(grp >> 1, tok) << 4) + (grp & 1) * 8;
   const uint8_t sb = base[(isv ? kOffVs : kOffKs) + grp * kPageTokens + tok];
   const uint2 c = *reinterpret_cast<const uint2*>(codes);
   const uint2 d0 = dequant8(c.x, s_tab[sb]), d1 = dequant8(c.y, s_tab[sb]);

@@ -90,7 +90,9 @@ __global__ void __launch_bounds__(256) quantize_insert_kernel(
     uint8_t* head = kv_pool + (size_t)page * kKvPageBytes + g * kHeadBytes;
     const int off_c = is_v ? kOffVc : kOffKc;
     const int off_s = is_v ? kOffVs : kOffKs;
-    *reinterpret_cast<uint16_t*>(head + off_c + off * 64 + lane * 2) = packed;
+    // lane l's two bytes: offset 2l & 15 of code chunk l >> 3
+    *reinterpret_cast<uint16_t*>(head + off_c + off * 64 + (code_chunk_pos(lane >> 3, off) << 4) +
+                                 ((lane & 7) << 1)) = packed;
     if ((lane & 3) == 0) head[off_s + (lane >> 2) * kPageTokens + off] = (uint8_t)sb_byte;
   }
 }

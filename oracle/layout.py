@@ -10,9 +10,11 @@ placement of bytes inside a page is this library's own format, restated here
 independently of the CUDA code from its written specification:
 
 KV page, 73,728 bytes = 4 heads x 18,432 bytes; head g starts at g * 18,432:
-    +0      K codes   [128 tokens][64 B]  byte i = code(2i) | code(2i+1) << 4
+    +0      K codes   [128 tokens][64 B]  byte i = code(2i) | code(2i+1) << 4,
+            except that the 16-byte chunk c of token t's row (channels
+            32c..32c+31) is stored at chunk position c XOR ((t >> 1) mod 4)
     +8,192  K scales  [8 groups][128 tokens]   E4M3, group k = channels 16k..16k+15
-    +9,216  V codes   [128 tokens][64 B]
+    +9,216  V codes   [128 tokens][64 B], chunks placed like the K codes
     +17,408 V scales  [8 groups][128 tokens]
 Index page, 16,384 bytes = [128 tokens][128 B] E4M3 index keys, where the
 16-byte chunk c of token t's row (dims 16c..16c+15) is stored at chunk
@@ -49,6 +51,11 @@ def unpack_codes(packed):
     return out
 
 
+def code_chunk_position(c, t):
+    """Chunk position of the 16-byte code chunk c in token t's 64-byte row."""
+    return c ^ ((t >> 1) % 4)
+
+
 def write_kv_slot(pool, page, t, k_codes, k_scales, v_codes, v_scales):
     """Write one token's NVFP4 K/V (codes [4,128], scales [4,8]) into slot t of a page.
 
@@ -59,7 +66,10 @@ def write_kv_slot(pool, page, t, k_codes, k_scales, v_codes, v_scales):
         for off_c, off_s, codes, scales in ((OFF_KC, OFF_KS, k_codes, k_scales),
                                             (OFF_VC, OFF_VS, v_codes, v_scales)):
             row = base + off_c + t * 64
-            pool[page, row:row + 64] = pack_codes(codes[g])
+            packed = pack_codes(codes[g])
+            for c in range(4):
+                pos = code_chunk_position(c, t)
+                pool[page, row + 16 * pos:row + 16 * pos + 16] = packed[16 * c:16 * c + 16]
             for k in range(8):
                 pool[page, base + off_s + k * PAGE_TOKENS + t] = scales[g][k]
 
@@ -82,7 +92,11 @@ def read_kv_slot(pool, page, t):
         for g in range(KV_HEADS):
             base = g * HEAD_BYTES
             row = base + off_c + t * 64
-            codes[g] = unpack_codes(pool[page, row:row + 64])
+            packed = np.zeros(64, dtype=np.uint8)
+            for c in range(4):
+                pos = code_chunk_position(c, t)
+                packed[16 * c:16 * c + 16] = pool[page, row + 16 * pos:row + 16 * pos + 16]
+            codes[g] = unpack_codes(packed)
             for k in range(8):
                 scales[g, k] = pool[page, base + off_s + k * PAGE_TOKENS + t]
         out += [codes, scales]
