@@ -207,7 +207,8 @@ int msa_indexer_topk_noalloc(const msa_cache* cache, const uint8_t* q_idx, const
  *               the split's logits (-inf for an empty split).
  * Per element the FP8 operand is sign(code) | E4M3_RNE(|e2m1(code)| * sb);
  * logits = (q . k8) * softmax_scale / s_enc_k; the value contraction is
- * divided by s_enc_v.  Keys after pos_j are masked.
+ * divided by s_enc_v.  Keys after pos_j are masked.  Limits: n_seqs <= 4096,
+ * n_q_total <= 65535 (else MSA_ERR_UNSUPPORTED_SHAPE).
  */
 int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q_heads,
                            float softmax_scale, const int32_t* sel, const int32_t* n_sel,

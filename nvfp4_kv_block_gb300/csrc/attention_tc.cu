@@ -1,5 +1,6 @@
 // Split-context sparse GQA attention over the selected NVFP4 blocks on the
-// fifth-generation tensor cores (tcgen05, tensor memory), warp-specialised.
+// fifth-generation tensor cores (tcgen05, tensor memory): one persistent,
+// warp-specialised CTA per SM.
 //
 // "vLLM Delivers Day-0 Support for MiniMax-M3.1-Flash" blog, section "Sparse
 // attention still scans an index": exact attention over the selected blocks
@@ -7,59 +8,87 @@
 // article (third paragraph): queries stay FP8, so the NVFP4 K/V are converted
 // to FP8 before the matrix multiply.
 //
-// One CTA = (split, KV head, query token); two CTAs per SM.  The split's pages
-// flow through a pipeline of warp roles, each hand-off an mbarrier:
-//   warp 0      TMA producer: one 18 KB cp.async.bulk per (page, head) block
-//               (K/V codes and scales) into a 2-stage ring;
-//   warps 6-9   conversion, thread = token: NVFP4 K and V rows -> FP8 through a
-//               256-entry shared table of scaled E4M3 values and byte permutes,
-//               written as 128-byte-swizzled tiles (K8, V8; two of each);
-//   warp 1      MMA issuer: S = K8 Q^T (tcgen05.mma kind::f8f6f4, M = 128
-//               tokens, N = 16: the 4 query heads of this KV head, zero padded,
-//               K = 128 channels) into one of two TMEM S buffers, and
-//               O^T = V8^T P (A = the V tile read MN-major, no transpose) into
-//               one of two TMEM O buffers; QK of page e+1 is issued before PV of
-//               page e, so the softmax of e+1 overlaps PV(e);
-//   warps 2-5   softmax, thread = token row of S: page max per head, P = exp2
-//               relative to the page max, scaled by 2^8 and split into two E4M3
-//               terms (value + rounding remainder) as the B operand of PV; then
-//               thread = channel: the page's O folded into the running
-//               (m, l, o) state, O of the split normalised at the end.
-// Every wait is bounded; a timeout raises MSA_STATUS_TIMEOUT and the split's
-// output is written as empty.  The LSE merge kernel combines the splits.
+// Work item = (query token j, KV head, split): the split's share of j's
+// selected pages (entries split, split + S, ... of its selection).  CTA c
+// takes items c, c + G, c + 2G, ...; its pages (numbered e = 0, 1, ... across
+// its items) flow through warp roles, every hand-off an mbarrier and every
+// wait bounded:
+//   warp 0       scheduler: per item, the sequence of j (shared-memory copy of
+//                q_start_loc), the selected blocks, their physical pages and the
+//                tokens visible in each, and the 4 query rows as a swizzled
+//                tile, into a 4-deep ring of item records;
+//   warp 1       TMA producer: per page two 9 KB cp.async.bulk copies, the K
+//                half (codes + scales) and the V half, into two 6-stage rings;
+//   warps 12-15  K conversion, thread = token: NVFP4 -> FP8 through a 256-entry
+//                shared table of scaled E4M3 values and byte permutes, written
+//                with tcgen05.st straight into tensor memory (the A operand);
+//   warps 16-19  V conversion, thread = token: the same into a 128-byte-swizzled
+//                shared-memory tile (3 tiles);
+//   warp 2       QK issuer: S = K8 Q^T (kind::f8f6f4, M = 128 tokens, N = 16: the
+//                4 query heads, zero padded, K = 128, A from tensor memory);
+//   warp 3       PV issuer: O^T = V8^T P (A = the V tile read MN-major, no
+//                transpose, B = P), one of 4 TMEM O buffers per page;
+//   warps 4-11   softmax, two sets of 4 warps; set s takes the pages with
+//                e % 2 == s and keeps its own running (m, l, o): thread = token
+//                row of S: page max per head, P = exp2 relative to the page max,
+//                scaled by 2^8 and split into two E4M3 terms (value + rounding
+//                remainder) as the B operand of PV; thread = channel: the page's
+//                O folded into the running state.  At the item's end set 1 hands
+//                its state to set 0, which merges the two and writes the
+//                normalised partial (O, LSE).  The LSE merge kernel combines the
+//                splits.
 #include "common.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kThreads = 320;  // 10 warps
-constexpr int kTileBytes = 16384;                      // [128 rows][128 B], swizzled
-constexpr int kOffK8 = 0;                              // 2 K8 tiles
-constexpr int kOffV8 = 2 * kTileBytes;                 // 2 V8 tiles
-constexpr int kOffQ = 4 * kTileBytes;                  // [16 rows][128 B]: Q rows 0-3
-constexpr int kOffP = kOffQ + 2048;                    // 2 x [16 rows][128 B]: P hi 0-3, lo 4-7
-constexpr int kOffRaw = kOffP + 2 * 2048;              // 2 x 18,432 (K/V codes + scales)
-constexpr int kOffTab = kOffRaw + 2 * kHeadBytes;      // uint2 [256] dequant table
-constexpr int kOffBars = kOffTab + 2048;               // 25 mbarriers
-constexpr int kNumBars = 25;
-constexpr int kOffMisc = kOffBars + kNumBars * 8;      // tmem slot, seq, abort, n pages, issued
-constexpr int kOffRed = kOffMisc + 32;                 // float [2][4 warps][4 heads] page maxima
-constexpr int kOffRedL = kOffRed + 128;                // float [4 warps][4 heads] row sums
-constexpr int kOffSel = kOffRedL + 64;                 // int [17] phys, [17] valid, [17] block
-constexpr int kSmemBytes = kOffSel + 3 * kSelStride * 4;
-constexpr int kSmemAlloc = kSmemBytes + 1024;          // + alignment slack
-constexpr uint32_t kTmemCols = 64;                     // S: 0, 16; O: 32, 48
+constexpr int kThreads = 640;  // 20 warps
+constexpr int kStages = 6;     // raw K and raw V ring depth
+constexpr int kRecs = 4;       // item records in flight
+constexpr int kV8Tiles = 3;
+constexpr int kPO = 4;         // P tiles and O buffers
+constexpr int kHalfBytes = kHeadBytes / 2;  // 9,216: codes + scales of K (or V)
+constexpr int kTileBytes = 16384;           // [128 rows][128 B], swizzled
+constexpr int kOffV8 = 0;                                   // kV8Tiles V8 tiles
+constexpr int kOffQ = kV8Tiles * kTileBytes;                // kRecs x [16 rows][128 B]
+constexpr int kOffP = kOffQ + kRecs * 2048;                 // kPO x [16 rows][128 B]
+constexpr int kOffKRaw = kOffP + kPO * 2048;                // kStages x 9,216
+constexpr int kOffVRaw = kOffKRaw + kStages * kHalfBytes;   // kStages x 9,216
+constexpr int kOffTab = kOffVRaw + kStages * kHalfBytes;    // uint2 [256]
+constexpr int kOffRec = kOffTab + 2048;                     // kRecs x 256 B
+constexpr int kOffMerge = kOffRec + kRecs * 256;            // 2 x (o [4][128], m [4], L [4]) floats
+constexpr int kMergeBytes = (4 * 128 + 8) * 4;
+constexpr int kOffBars = kOffMerge + 2 * kMergeBytes;
+// barrier indices
+constexpr int kKrFull = 0, kKrEmpty = kStages, kVrFull = 2 * kStages, kVrEmpty = 3 * kStages;
+constexpr int kK8Full = 4 * kStages, kK8Empty = kK8Full + 2, kSFull = kK8Full + 4,
+              kSEmpty = kK8Full + 6, kV8Full = kK8Full + 8, kV8Empty = kV8Full + kV8Tiles,
+              kPFull = kV8Empty + kV8Tiles, kPEmpty = kPFull + kPO, kOFull = kPEmpty + kPO,
+              kOEmpty = kOFull + kPO, kRecFull = kOEmpty + kPO, kRecEmpty = kRecFull + kRecs,
+              kMergeFull = kRecEmpty + kRecs, kMergeEmpty = kMergeFull + 2, kDone = kMergeEmpty + 2,
+              kNumBars = kDone + 2;  // kDone: QK issuer, kDone + 1: PV issuer
+constexpr int kOffMisc = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;  // tmem, abort, issued K/V
+constexpr int kOffRed = kOffMisc + 16;        // float [2 sets][2][4 warps][4 heads] page maxima
+constexpr int kOffRedL = kOffRed + 256;       // float [2 sets][4 warps][4 heads] row sums
+constexpr int kOffQsl = kOffRedL + 128;       // int [n_seqs + 1] copy of q_start_loc
+constexpr uint32_t kTmemCols = 256;           // K8: 0, 32; S: 64, 80; O: 96 + 16 i
+constexpr int kRecEmptyCount = 1 + 4 + 4 + 1 + 1 + 8;  // producer, K, V, QK, PV, softmax
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1 KB alignment");
-static_assert(kOffRaw % 16 == 0 && kOffTab % 8 == 0 && kOffBars % 8 == 0, "alignment");
-static_assert(2 * (kSmemAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(kOffKRaw % 16 == 0 && kOffVRaw % 16 == 0 && kHalfBytes % 16 == 0, "bulk copy alignment");
+static_assert(kOffMerge % 16 == 0, "alignment");
 
-// barrier indices; slot s of each pair is index + s
-enum : int {
-  kRawFull = 0, kRawEmpty = 2, kK8Full = 4, kK8Empty = 6, kV8Full = 8, kV8Empty = 10,
-  kSFull = 12, kSEmpty = 14, kPFull = 16, kPEmpty = 18, kOFull = 20, kOEmpty = 22, kDone = 24
+size_t attn_smem_bytes(int n_seqs) { return 1024 + kOffQsl + 4 * (size_t)(n_seqs + 1); }
+
+// One item record (256 bytes of shared memory).
+struct ItemRec {
+  int n_pg;                // pages of the item after dropping invalid entries
+  int j, kvh, split;
+  int phys[kSelStride];    // physical page of each
+  int valid[kSelStride];   // tokens of the page visible to j (128 except the recent block)
 };
+static_assert(sizeof(ItemRec) <= 256, "record slot");
 
 struct AttnParams {
   const uint8_t* kv_pool;
@@ -74,6 +103,7 @@ struct AttnParams {
   int n_seqs;
   int n_q_total;
   int n_splits;
+  int n_items;       // T * 4 * n_splits
   float scale_log2;  // softmax_scale / s_enc_k * log2(e)
   float out_scale;   // 1 / (256 * s_enc_v)
   float* o_part;     // [T][S][16][128]
@@ -93,352 +123,497 @@ __device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred
   return r != 0;
 }
 
-// Converts one token row -- 64 code bytes, 8 scale groups -- to 128 FP8 bytes in
-// row `row` of a 128-byte-swizzled tile (16-byte chunk j at position j ^ (row & 7)).
-// Code chunk c sits at position c ^ ((row >> 1) & 3) of the row, so the 16-byte
-// loads of 8 consecutive rows (64 B apart) hit 8 different bank groups; the
-// tile stores of 8 consecutive rows do too.
-__device__ __forceinline__ void convert_row(const uint8_t* codes, const uint8_t* scales_col,
-                                            const uint2* tab, uint8_t* tile, int row, bool live) {
-  uint8_t* dst = tile + row * 128;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint4 w = *reinterpret_cast<const uint4*>(codes + 16 * code_chunk_pos(c, row));
-    // 16 code bytes = channels 32c..32c+31 = groups 2c and 2c+1
-    const uint2 t0 = tab[scales_col[(2 * c) * kPageTokens]];
-    const uint2 t1 = tab[scales_col[(2 * c + 1) * kPageTokens]];
-    const uint2 a = dequant8(w.x, t0), b = dequant8(w.y, t0);
-    const uint2 d = dequant8(w.z, t1), e = dequant8(w.w, t1);
-    uint4 o0 = make_uint4(a.x, a.y, b.x, b.y), o1 = make_uint4(d.x, d.y, e.x, e.y);
-    if (!live) o0 = o1 = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (row & 7)) << 4)) = o0;
-    *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (row & 7)) << 4)) = o1;
-  }
+// Every lane of the warp waits; the result is the same for all of them.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
-__global__ void __launch_bounds__(kThreads, 2) sparse_attn_tc_kernel(AttnParams p) {
+// Code chunk c (32 channels) of token `row`: 16 code bytes and the two group
+// scales -> 32 FP8 bytes (channels 32c..32c+31) in o[0..7], zeros for a token
+// after pos_j (live false).  Code chunk c sits at position c ^ ((row >> 1) & 3),
+// so chunk c of 8 consecutive rows (64 B apart) lies in 8 different bank groups.
+__device__ __forceinline__ void convert_chunk(const uint8_t* raw, const uint2* tab, int row, int c,
+                                              bool live, uint32_t* o) {
+  const uint4 w = *reinterpret_cast<const uint4*>(raw + row * 64 + 16 * code_chunk_pos(c, row));
+  const uint8_t* sc = raw + kOffKs + row;  // scales [8 groups][128 tokens] after the codes
+  const uint2 t0 = tab[sc[(2 * c) * kPageTokens]];
+  const uint2 t1 = tab[sc[(2 * c + 1) * kPageTokens]];
+  const uint2 a = dequant8(w.x, t0), b = dequant8(w.y, t0);
+  const uint2 d = dequant8(w.z, t1), e = dequant8(w.w, t1);
+  o[0] = live ? a.x : 0u; o[1] = live ? a.y : 0u; o[2] = live ? b.x : 0u; o[3] = live ? b.y : 0u;
+  o[4] = live ? d.x : 0u; o[5] = live ? d.y : 0u; o[6] = live ? e.x : 0u; o[7] = live ? e.y : 0u;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) { return sbase + kOffBars + 8 * i; };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  int* s_seq = reinterpret_cast<int*>(smem + kOffMisc + 4);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
-  int* s_npg = reinterpret_cast<int*>(smem + kOffMisc + 12);
-  int* s_issued = reinterpret_cast<int*>(smem + kOffMisc + 16);
-  float* s_red = reinterpret_cast<float*>(smem + kOffRed);
-  float* s_redl = reinterpret_cast<float*>(smem + kOffRedL);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* s_issued_k = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  int* s_issued_v = reinterpret_cast<int*>(smem + kOffMisc + 12);
   uint2* s_tab = reinterpret_cast<uint2*>(smem + kOffTab);
-  int* s_phys = reinterpret_cast<int*>(smem + kOffSel);
-  int* s_valid = s_phys + kSelStride;
-  int* s_blk = s_valid + kSelStride;
+  int* s_qsl = reinterpret_cast<int*>(smem + kOffQsl);
+  auto rec = [&](int slot) { return reinterpret_cast<ItemRec*>(smem + kOffRec + 256 * slot); };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int split = blockIdx.x, kvh = blockIdx.y, j = blockIdx.z;
+  const int G = gridDim.x;
+  // items of this CTA: blockIdx.x + k * G for k < n_mine
+  const int n_mine = p.n_items > (int)blockIdx.x ? (p.n_items - 1 - (int)blockIdx.x) / G + 1 : 0;
 
-  // ---- prologue that needs no input of the previous kernel -------------------
+  // ---- prologue ------------------------------------------------------------------
   build_dequant_table(s_tab, tid, kThreads);
   if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(kKrFull + i), 1);
+      mbar_init(bar(kKrEmpty + i), 4);
+      mbar_init(bar(kVrFull + i), 1);
+      mbar_init(bar(kVrEmpty + i), 4);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kRawFull + i), 1);
-      mbar_init(bar(kRawEmpty + i), 4);
       mbar_init(bar(kK8Full + i), 4);
       mbar_init(bar(kK8Empty + i), 1);
-      mbar_init(bar(kV8Full + i), 4);
-      mbar_init(bar(kV8Empty + i), 1);
       mbar_init(bar(kSFull + i), 1);
       mbar_init(bar(kSEmpty + i), 4);
+      mbar_init(bar(kMergeFull + i), 4);
+      mbar_init(bar(kMergeEmpty + i), 4);
+    }
+    for (int i = 0; i < kV8Tiles; ++i) {
+      mbar_init(bar(kV8Full + i), 4);
+      mbar_init(bar(kV8Empty + i), 1);
+    }
+    for (int i = 0; i < kPO; ++i) {
       mbar_init(bar(kPFull + i), 4);
       mbar_init(bar(kPEmpty + i), 1);
       mbar_init(bar(kOFull + i), 1);
       mbar_init(bar(kOEmpty + i), 4);
     }
+    for (int i = 0; i < kRecs; ++i) {
+      mbar_init(bar(kRecFull + i), 1);
+      mbar_init(bar(kRecEmpty + i), kRecEmptyCount);
+    }
     mbar_init(bar(kDone), 1);
-    *s_seq = -1;
+    mbar_init(bar(kDone + 1), 1);
     *s_abort = 0;
-    *s_issued = 0;
+    *s_issued_k = 0;
+    *s_issued_v = 0;
     fence_barrier_init();
   }
-  // zero the Q tile and both P tiles (the rows that stay zero pad N to 16)
-  for (int i = tid; i < 3 * 2048 / 16; i += kThreads)
+  // zero the Q tiles and the P tiles (rows that stay zero pad N to 16)
+  for (int i = tid; i < (kRecs + kPO) * 2048 / 16; i += kThreads)
     reinterpret_cast<uint4*>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
-  if (warp == 1) tmem_alloc(smem_u32(s_tmem), kTmemCols);
-  __syncthreads();  // s_seq = -1 is in place before any thread records a match
-  // sequence of token j: the b with q_start_loc[b] <= j < q_start_loc[b+1]
-  for (int base = 0; base < p.n_seqs; base += kThreads) {
-    const int b = base + tid;
-    if (b < p.n_seqs && p.q_start_loc[b] <= j && j < p.q_start_loc[b + 1]) *s_seq = b;
-  }
+  // q_start_loc does not come from the previous kernel
+  for (int i = tid; i <= p.n_seqs; i += kThreads) s_qsl[i] = p.q_start_loc[i];
+  if (warp == 2) tmem_alloc(smem_u32(s_tmem), kTmemCols);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const int b = *s_seq;
-  SeqInfo s{0, 0, 0, false};
-  if (b >= 0) s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
-  const bool seq_ok = b >= 0 && s.ok;
-  const int pos = s.seq_len - s.n_q + (j - s.q0);
-  const int r_blk = seq_ok ? pos / kPageTokens : -1;
-  if (tid < 32) {  // query rows 0-3: heads 4*kvh .. 4*kvh+3, 128-byte swizzled K-major
-    const int row = tid >> 3, c = tid & 7;
-    const uint4 v = *reinterpret_cast<const uint4*>(p.q + ((size_t)j * kQHeads + kvh * kGqa + row) * kHeadDim + 16 * c);
-    *reinterpret_cast<uint4*>(smem + kOffQ + row * 128 + ((c ^ row) << 4)) = v;
-  }
-
   pdl_wait();  // the selection comes from the indexer kernel
-  const int nsel = seq_ok ? min(p.n_sel[j], kSelStride) : 0;
-  if (tid < kSelStride) {
-    const int e = split + tid * p.n_splits;
-    int blk = -1, phys = -1;
-    if (e < nsel) {
-      blk = p.sel[(size_t)j * kSelStride + e];
-      if (blk < 0 || blk > r_blk) {
-        set_status(p.status, MSA_STATUS_BAD_SELECTION);
-      } else {
-        phys = p.block_table[(size_t)b * p.max_pages + blk];
-        if (phys < 0 || phys >= p.n_pages) {
-          set_status(p.status, MSA_STATUS_BAD_PAGE);
-          phys = -1;
-        }
-      }
-    }
-    s_blk[tid] = blk;
-    s_phys[tid] = phys;
-  }
-  if (tid == 0 && !seq_ok) set_status(p.status, MSA_STATUS_BAD_SEQ);
-  fence_proxy_async_smem();  // Q rows and zero rows -> visible to the tensor core
-  __syncthreads();
   pdl_trigger();
-  if (tid == 0) {  // compact this split's valid pages; tokens visible in each
-    int n = 0;
-    for (int i = 0; i < kSelStride; ++i)
-      if (s_phys[i] >= 0) {
-        s_phys[n] = s_phys[i];
-        s_valid[n] = s_blk[i] == r_blk ? (pos % kPageTokens) + 1 : kPageTokens;
-        ++n;
-      }
-    *s_npg = n;
-  }
-  __syncthreads();
-  const int n_pg = *s_npg;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------------------------------------
+    // ---------------- scheduler: item records ------------------------------------------
+    for (int k = 0; k < n_mine; ++k) {
+      const int slot = k % kRecs;
+      if (!warp_wait(bar(kRecEmpty + slot), ((k / kRecs) & 1) ^ 1, s_abort)) break;
+      const int item = blockIdx.x + k * G;
+      const int split = item % p.n_splits, kvh = (item / p.n_splits) % kKvHeads;
+      const int j = item / (p.n_splits * kKvHeads);
+      // sequence b of token j: the last b with q_start_loc[b] <= j (binary search)
+      int lo = 0, hi = p.n_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_qsl[mid] <= j) lo = mid; else hi = mid - 1;
+      }
+      const int b = p.n_seqs > 0 ? lo : -1;
+      // first round of loads, all independent: sequence length, selection, query rows
+      const int seq_len = b >= 0 ? p.seq_lens[b] : 0;
+      const int nsel_raw = p.n_sel[j];
+      const int e_sel = split + lane * p.n_splits;
+      const int blk_raw = lane < kSelStride && e_sel < kSelStride ? p.sel[(size_t)j * kSelStride + e_sel] : -1;
+      const uint4 qv = *reinterpret_cast<const uint4*>(
+          p.q + ((size_t)j * kQHeads + kvh * kGqa + (lane >> 3)) * kHeadDim + 16 * (lane & 7));
+      const int q0 = b >= 0 ? s_qsl[b] : 0, n_q = b >= 0 ? s_qsl[b + 1] - q0 : 0;
+      const bool seq_ok = b >= 0 && q0 <= j && j < q0 + n_q && q0 >= 0 && q0 + n_q <= p.n_q_total &&
+                          seq_len >= n_q && seq_len <= p.max_pages * kPageTokens;
+      const int pos = seq_len - n_q + (j - q0);
+      const int r_blk = seq_ok ? pos / kPageTokens : -1;
+      const int nsel = seq_ok ? min(nsel_raw, kSelStride) : 0;
+      int phys = -1;
+      if (lane < kSelStride && e_sel < nsel) {
+        if (blk_raw < 0 || blk_raw > r_blk) {
+          set_status(p.status, MSA_STATUS_BAD_SELECTION);
+        } else {
+          phys = p.block_table[(size_t)b * p.max_pages + blk_raw];  // second round
+          if (phys < 0 || phys >= p.n_pages) {
+            set_status(p.status, MSA_STATUS_BAD_PAGE);
+            phys = -1;
+          }
+        }
+      }
+      if (lane == 0 && !seq_ok) set_status(p.status, MSA_STATUS_BAD_SEQ);
+      // compact the valid entries (order kept)
+      const unsigned okmask = __ballot_sync(0xffffffffu, phys >= 0);
+      ItemRec* r = rec(slot);
+      if (phys >= 0) {
+        const int at = __popc(okmask & ((1u << lane) - 1));
+        r->phys[at] = phys;
+        r->valid[at] = blk_raw == r_blk ? (pos % kPageTokens) + 1 : kPageTokens;
+      }
+      if (lane == 0) {
+        r->n_pg = __popc(okmask);
+        r->j = j;
+        r->kvh = kvh;
+        r->split = split;
+      }
+      // query rows 0-3 (heads 4 kvh .. 4 kvh + 3), 128-byte swizzled K-major
+      {
+        const int row = lane >> 3, c = lane & 7;
+        *reinterpret_cast<uint4*>(smem + kOffQ + slot * 2048 + row * 128 + ((c ^ row) << 4)) = qv;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kRecFull + slot));
+    }
+  } else if (warp == 1) {
+    // ---------------- TMA producer: K and V halves of every page -------------------------
     if (lane == 0) {
       int e = 0;
-      for (; e < n_pg; ++e) {
-        const int sl = e & 1;
-        if (!mbar_wait(bar(kRawEmpty + sl), ((e >> 1) & 1) ^ 1, s_abort)) break;
-        mbar_arrive_expect_tx(bar(kRawFull + sl), kHeadBytes);
-        bulk_g2s(sbase + kOffRaw + sl * kHeadBytes,
-                 p.kv_pool + (size_t)s_phys[e] * kKvPageBytes + kvh * kHeadBytes, kHeadBytes,
-                 bar(kRawFull + sl));
-      }
-      *s_issued = e;
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---------------- MMA issuer --------------------------------------------------
-    if (lane == 0) {
-      const uint32_t idesc_qk = umma_idesc_e4m3(128, 16);
-      const uint32_t idesc_pv = umma_idesc_e4m3_amn(128, 16);
-      const uint64_t qdesc = umma_desc_sw128(sbase + kOffQ);
-      auto qk = [&](int e) -> bool {
-        const int sl = e & 1, ph = (e >> 1) & 1;
-        if (!mbar_wait(bar(kK8Full + sl), ph, s_abort)) return false;
-        if (!mbar_wait(bar(kSEmpty + sl), ph ^ 1, s_abort)) return false;
-        tc_fence_after();
-        const uint64_t adesc = umma_desc_sw128(sbase + kOffK8 + sl * kTileBytes);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // K = 32 bytes per MMA: +32 B = +2 in the encoded address
-          umma_e4m3(tmem + 16 * sl, adesc + 2 * k, qdesc + 2 * k, idesc_qk, k > 0);
-        umma_commit(bar(kK8Empty + sl));
-        umma_commit(bar(kSFull + sl));
-        return true;
-      };
-      auto pv = [&](int e) -> bool {
-        const int sl = e & 1, ph = (e >> 1) & 1;
-        if (!mbar_wait(bar(kV8Full + sl), ph, s_abort)) return false;
-        if (!mbar_wait(bar(kPFull + sl), ph, s_abort)) return false;
-        if (!mbar_wait(bar(kOEmpty + sl), ph ^ 1, s_abort)) return false;
-        tc_fence_after();
-        const uint64_t bdesc = umma_desc_sw128(sbase + kOffP + sl * 2048);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          // A: V tile read MN-major; 32 tokens (4 swizzle atoms of 8 rows) per MMA
-          const uint64_t adesc =
-              umma_desc_sw128_lbo_sbo(sbase + kOffV8 + sl * kTileBytes + k * 4096, 1024, 1024);
-          umma_e4m3(tmem + 32 + 16 * sl, adesc, bdesc + 2 * k, idesc_pv, k > 0);
+      bool ok = true;
+      for (int k = 0; ok && k < n_mine; ++k) {
+        const int slot = k % kRecs;
+        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort)) break;
+        const ItemRec* r = rec(slot);
+        const int n = r->n_pg;
+        const uint8_t* head = p.kv_pool + (size_t)r->kvh * kHeadBytes;
+        for (int i = 0; i < n; ++i, ++e) {
+          const int st = e % kStages, ph = (e / kStages) & 1;
+          const uint8_t* src = head + (size_t)r->phys[i] * kKvPageBytes;
+          if (!mbar_wait(bar(kKrEmpty + st), ph ^ 1, s_abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(kKrFull + st), kHalfBytes);
+          bulk_g2s(sbase + kOffKRaw + st * kHalfBytes, src, kHalfBytes, bar(kKrFull + st));
+          *s_issued_k = e + 1;
+          if (!mbar_wait(bar(kVrEmpty + st), ph ^ 1, s_abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(kVrFull + st), kHalfBytes);
+          bulk_g2s(sbase + kOffVRaw + st * kHalfBytes, src + kHalfBytes, kHalfBytes, bar(kVrFull + st));
+          *s_issued_v = e + 1;
         }
-        umma_commit(bar(kV8Empty + sl));
-        umma_commit(bar(kPEmpty + sl));
-        umma_commit(bar(kOFull + sl));
-        return true;
-      };
-      bool ok = n_pg == 0 || qk(0);
-      for (int e = 0; ok && e < n_pg; ++e) {
-        if (e + 1 < n_pg && !qk(e + 1)) break;
-        if (!pv(e)) break;
-      }
-      if (*s_abort) {
-        // no tcgen05.mma may still be running when tensor memory is released
-        volatile int ignore = 0;
-        umma_commit(bar(kDone));
-        mbar_wait(bar(kDone), 0, &ignore);
+        if (ok) mbar_arrive(bar(kRecEmpty + slot));
       }
     }
     __syncwarp();
-  } else if (warp >= 6) {
-    // ---------------- conversion: thread = token --------------------------------
-    const int tok = tid - 192;
-    for (int e = 0; e < n_pg; ++e) {
-      const int sl = e & 1, ph = (e >> 1) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kRawFull + sl), ph, s_abort))) break;
-      const bool live = tok < s_valid[e];
-      const uint8_t* raw = smem + kOffRaw + sl * kHeadBytes;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kK8Empty + sl), ph ^ 1, s_abort))) break;
-      convert_row(raw + kOffKc + tok * 64, raw + kOffKs + tok, s_tab, smem + kOffK8 + sl * kTileBytes, tok, live);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kK8Full + sl));
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kV8Empty + sl), ph ^ 1, s_abort))) break;
-      convert_row(raw + kOffVc + tok * 64, raw + kOffVs + tok, s_tab, smem + kOffV8 + sl * kTileBytes, tok, live);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(kV8Full + sl));
-        mbar_arrive(bar(kRawEmpty + sl));
+  }
+  else if (warp == 2) {
+    // ---------------- QK issuer ---------------------------------------------------------------
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_e4m3(128, 16);
+      int e = 0;
+      bool ok = true;
+      for (int k = 0; ok && k < n_mine; ++k) {
+        const int slot = k % kRecs;
+        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort)) break;
+        const int n = rec(slot)->n_pg;
+        const uint64_t bdesc = umma_desc_sw128(sbase + kOffQ + slot * 2048);
+        for (int i = 0; i < n; ++i, ++e) {
+          const int sl = e & 1, ph = (e >> 1) & 1;
+          if (!mbar_wait(bar(kK8Full + sl), ph, s_abort) || !mbar_wait(bar(kSEmpty + sl), ph ^ 1, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 32 per MMA: 8 TMEM columns of A, +32 B (+2) of B
+            umma_e4m3_ts(tmem + 64 + 16 * sl, tmem + 32 * sl + 8 * kk, bdesc + 2 * kk, idesc, kk > 0);
+          umma_commit(bar(kK8Empty + sl));
+          umma_commit(bar(kSFull + sl));
+        }
+        if (!ok) break;
+        // the record's Q tile is free once these MMAs are done
+        if (n > 0) umma_commit(bar(kRecEmpty + slot));
+        else mbar_arrive(bar(kRecEmpty + slot));
       }
+      umma_commit(bar(kDone));  // arrives when every MMA of this thread is done
     }
-  } else {
-    // ---------------- softmax and O folding (warps 2-5) -------------------------
-    // warp w reads TMEM lanes 32 (w % 4) ..: row = token of S, channel of O
-    const int quad = warp & 3, row = 32 * quad + lane;
-    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
-    float m_run[4], l_run[4], o_run[4], a_prev[4], b_prev[4];
+    __syncwarp();
+  } else if (warp == 3) {
+    // ---------------- PV issuer ---------------------------------------------------------------
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_e4m3_amn(128, 16);
+      int e = 0;
+      bool ok = true;
+      for (int k = 0; ok && k < n_mine; ++k) {
+        const int slot = k % kRecs;
+        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort)) break;
+        const int n = rec(slot)->n_pg;
+        mbar_arrive(bar(kRecEmpty + slot));  // nothing else of the record is needed
+        for (int i = 0; i < n; ++i, ++e) {
+          const int v = e % kV8Tiles, vph = (e / kV8Tiles) & 1, po = e & 3, pph = (e >> 2) & 1;
+          if (!mbar_wait(bar(kV8Full + v), vph, s_abort) || !mbar_wait(bar(kPFull + po), pph, s_abort) ||
+              !mbar_wait(bar(kOEmpty + po), pph ^ 1, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bdesc = umma_desc_sw128(sbase + kOffP + po * 2048);
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      m_run[h] = -INFINITY;
-      l_run[h] = 0.f;
-      o_run[h] = 0.f;
-      a_prev[h] = 1.f;
-      b_prev[h] = 0.f;
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: V tile read MN-major; 32 tokens (4 swizzle atoms of 8 rows) per MMA
+            const uint64_t adesc =
+                umma_desc_sw128_lbo_sbo(sbase + kOffV8 + v * kTileBytes + kk * 4096, 1024, 1024);
+            umma_e4m3(tmem + 96 + 16 * po, adesc, bdesc + 2 * kk, idesc, kk > 0);
+          }
+          umma_commit(bar(kV8Empty + v));
+          umma_commit(bar(kPEmpty + po));
+          umma_commit(bar(kOFull + po));
+        }
+      }
+      umma_commit(bar(kDone + 1));
     }
-    // O of page e (relative to its page max) -> running state
-    auto fold = [&](int e) -> bool {
-      const int sl = e & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kOFull + sl), (e >> 1) & 1, s_abort))) return false;
-      tc_fence_after();
-      float ov[8];
-      tmem_ld8(trow + 32 + 16 * sl, ov);  // columns 0-3: hi terms, 4-7: remainders
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kOEmpty + sl));
-#pragma unroll
-      for (int h = 0; h < 4; ++h) o_run[h] = o_run[h] * a_prev[h] + (ov[h] + ov[4 + h]) * b_prev[h];
-      return true;
-    };
+    __syncwarp();
+  } else if (warp >= 12) {
+    // ---------------- conversion: K (warps 12-15) or V (warps 16-19), thread = token ----
+    const bool is_k = warp < 16;
+    // K warps write TMEM lanes 32 (warp % 4) ..; V warps any order
+    const int tok = 32 * (warp & 3) + lane;
+    const int full0 = is_k ? kKrFull : kVrFull, empty0 = is_k ? kKrEmpty : kVrEmpty;
+    const uint32_t raw0 = is_k ? kOffKRaw : kOffVRaw;
+    int e = 0;
     bool ok = true;
-    for (int e = 0; e < n_pg; ++e) {
-      const int sl = e & 1, ph = (e >> 1) & 1;
-      bool good = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + sl), ph, s_abort));
-      float sv[4] = {0.f, 0.f, 0.f, 0.f};
-      if (good) {
+    for (int k = 0; ok && k < n_mine; ++k) {
+      const int slot = k % kRecs;
+      if (!warp_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort)) break;
+      const ItemRec* r = rec(slot);
+      const int n = r->n_pg;
+      for (int i = 0; i < n; ++i, ++e) {
+        const int st = e % kStages;
+        // output slot: K8 buffer e % 2 (freed by QK(e-2)), V8 tile e % 3 (freed by PV(e-3))
+        const int os = is_k ? (e & 1) : e % kV8Tiles;
+        const int oph = is_k ? ((e >> 1) & 1) : ((e / kV8Tiles) & 1);
+        if (!warp_wait(bar(full0 + st), (e / kStages) & 1, s_abort) ||
+            !warp_wait(bar((is_k ? kK8Empty : kV8Empty) + os), oph ^ 1, s_abort)) {
+          ok = false;
+          break;
+        }
+        const bool live = tok < r->valid[i];
+        const uint8_t* raw = smem + raw0 + st * kHalfBytes;
+        // K: row tok of A in TMEM, columns 32 os + 8c .. + 7 = channels 32c .. 32c + 31;
+        // V: row tok of the V tile, 16-byte chunk j at position j ^ (tok & 7)
+        const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * os;
+        uint8_t* dst = smem + kOffV8 + os * kTileBytes + tok * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[8];
+          convert_chunk(raw, s_tab, tok, c, live, o);
+          if (is_k) {
+            tmem_st8(ta + 8 * c, o);
+          } else {
+            *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (tok & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (tok & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        if (is_k) {
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar((is_k ? kK8Full : kV8Full) + os));
+          mbar_arrive(bar(empty0 + st));
+        }
+      }
+      if (ok && lane == 0) mbar_arrive(bar(kRecEmpty + slot));
+    }
+  }
+  else if (warp >= 4) {
+    // ---------------- softmax: set 0 = warps 4-7, set 1 = warps 8-11 ---------------------
+    // set s takes the pages with e % 2 == s; warp w reads TMEM lanes 32 (w % 4) ..:
+    // row = token of S, channel of O
+    const int set = (warp - 4) >> 2, quad = warp & 3, row = 32 * quad + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
+    const int nb = 1 + set;  // named barrier of the set
+    float* red = reinterpret_cast<float*>(smem + kOffRed) + set * 32;   // [2][4 warps][4 heads]
+    float* redl = reinterpret_cast<float*>(smem + kOffRedL) + set * 16;  // [4 warps][4 heads]
+    int e0 = 0;  // page number of the item's first page
+    bool ok = true;
+    for (int k = 0; ok && k < n_mine; ++k) {
+      const int slot = k % kRecs;
+      if (named_barrier_or(nb, 128, !warp_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort))) break;
+      const ItemRec* r = rec(slot);
+      const int n = r->n_pg;
+      float m_run[4], l_run[4], o_run[4], a_prev[4], b_prev[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        m_run[h] = -INFINITY;
+        l_run[h] = 0.f;
+        o_run[h] = 0.f;
+        a_prev[h] = 1.f;
+        b_prev[h] = 0.f;
+      }
+      // O of page ef (relative to its page max) -> running state
+      auto fold = [&](int ef) -> bool {
+        const int po = ef & 3;
+        if (!warp_wait(bar(kOFull + po), (ef >> 2) & 1, s_abort)) return false;
         tc_fence_after();
-        tmem_ld4(trow + 16 * sl, sv);
+        float ov[8];
+        tmem_ld8(trow + 96 + 16 * po, ov);  // columns 0-3: hi terms, 4-7: remainders
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kSEmpty + sl));
-      }
-      const bool live = row < s_valid[e];
-      float x[4];
+        if (lane == 0) mbar_arrive(bar(kOEmpty + po));
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        x[h] = live ? sv[h] * p.scale_log2 : -INFINITY;
-        const float wm = warp_max(x[h]);
-        if (lane == 0) s_red[(sl * 4 + quad) * 4 + h] = wm;
-      }
-      // page maxima complete; the four warps agree on whether to go on
-      if (named_barrier_or(1, 128, !good || !ok)) {
-        ok = false;
-        break;
-      }
-      uint32_t p_hi = 0, p_lo = 0;
-      float a_cur[4], b_cur[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float* r = s_red + sl * 16 + h;
-        const float mp = fmaxf(fmaxf(r[0], r[4]), fmaxf(r[8], r[12]));
-        const float m_new = fmaxf(m_run[h], mp);
-        // m_new = -inf only while no key so far is visible (then everything is 0)
-        a_cur[h] = m_new == -INFINITY ? 1.f : fast_exp2(m_run[h] - m_new);
-        b_cur[h] = mp == -INFINITY ? 0.f : fast_exp2(mp - m_new);  // page scale -> running scale
-        const float pr = mp == -INFINITY ? 0.f : fast_exp2(x[h] - mp);  // relative to the page max
-        l_run[h] = l_run[h] * a_cur[h] + pr * b_cur[h];
-        m_run[h] = m_new;
-        const float v256 = pr * 256.f;
-        const uint32_t hi = f32_to_e4m3(v256);
-        const uint32_t lo = f32_to_e4m3(v256 - e4m3_to_f32(hi));
-        p_hi |= hi << (8 * h);
-        p_lo |= lo << (8 * h);
-      }
-      // P rows h (E4M3 of 256 p) and 4+h (E4M3 of the remainder), one byte per
-      // token: byte t of row n sits in chunk (t/16) ^ (n & 7)
-      bool step_ok = __all_sync(0xffffffffu, mbar_wait(bar(kPEmpty + sl), ph ^ 1, s_abort));
-      if (step_ok) {
-        uint8_t* pt = smem + kOffP + sl * 2048;
+        for (int h = 0; h < 4; ++h) o_run[h] = o_run[h] * a_prev[h] + (ov[h] + ov[4 + h]) * b_prev[h];
+        return true;
+      };
+      int e_prev = -1;
+      for (int e = e0 + ((set - e0) & 1); e < e0 + n; e += 2) {
+        const int ph = (e >> 1) & 1;
+        bool good = warp_wait(bar(kSFull + set), ph, s_abort);
+        float sv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (good) {
+          tc_fence_after();
+          tmem_ld4(trow + 64 + 16 * set, sv);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kSEmpty + set));
+        }
+        const bool live = row < r->valid[e - e0];
+        float* rd = red + ph * 16;
+        float x[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          pt[h * 128 + (((row >> 4) ^ h) << 4) + (row & 15)] = (uint8_t)(p_hi >> (8 * h));
-          pt[(4 + h) * 128 + (((row >> 4) ^ (4 + h)) << 4) + (row & 15)] = (uint8_t)(p_lo >> (8 * h));
+          x[h] = live ? sv[h] * p.scale_log2 : -INFINITY;
+          const float wm = warp_max(x[h]);
+          if (lane == 0) rd[quad * 4 + h] = wm;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kPFull + sl));
-        if (e > 0) step_ok = fold(e - 1);
+        // page maxima complete; the set's four warps agree on whether to go on
+        if (named_barrier_or(nb, 128, !good || !ok)) {
+          ok = false;
+          break;
+        }
+        uint32_t p_hi = 0, p_lo = 0;
+        float a_cur[4], b_cur[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float mp = fmaxf(fmaxf(rd[h], rd[4 + h]), fmaxf(rd[8 + h], rd[12 + h]));
+          const float m_new = fmaxf(m_run[h], mp);
+          // m_new = -inf only while no key so far is visible (then everything is 0)
+          a_cur[h] = m_new == -INFINITY ? 1.f : fast_exp2(m_run[h] - m_new);
+          b_cur[h] = mp == -INFINITY ? 0.f : fast_exp2(mp - m_new);  // page scale -> running scale
+          const float pr = mp == -INFINITY ? 0.f : fast_exp2(x[h] - mp);  // relative to the page max
+          l_run[h] = l_run[h] * a_cur[h] + pr * b_cur[h];
+          m_run[h] = m_new;
+          const float v256 = pr * 256.f;
+          const uint32_t hi = f32_to_e4m3(v256);
+          const uint32_t lo = f32_to_e4m3(v256 - e4m3_to_f32(hi));
+          p_hi |= hi << (8 * h);
+          p_lo |= lo << (8 * h);
+        }
+        // P rows h (E4M3 of 256 p) and 4+h (E4M3 of the remainder), one byte per
+        // token: byte t of row n sits in chunk (t/16) ^ (n & 7)
+        const int po = e & 3;
+        bool step_ok = warp_wait(bar(kPEmpty + po), ((e >> 2) & 1) ^ 1, s_abort);
+        if (step_ok) {
+          uint8_t* pt = smem + kOffP + po * 2048;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            pt[h * 128 + (((row >> 4) ^ h) << 4) + (row & 15)] = (uint8_t)(p_hi >> (8 * h));
+            pt[(4 + h) * 128 + (((row >> 4) ^ (4 + h)) << 4) + (row & 15)] = (uint8_t)(p_lo >> (8 * h));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kPFull + po));
+          if (e_prev >= 0) step_ok = fold(e_prev);
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          a_prev[h] = a_cur[h];
+          b_prev[h] = b_cur[h];
+        }
+        e_prev = e;
+        ok = ok && step_ok;  // a failure here ends the loop at the next barrier
       }
+      if (ok && e_prev >= 0) ok = fold(e_prev);
+      const bool aborted = named_barrier_or(nb, 128, !ok || *s_abort != 0);
+      // ---- this set's sum of p over its tokens -------------------------------------------
+      float L[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        a_prev[h] = a_cur[h];
-        b_prev[h] = b_cur[h];
+        float l = l_run[h];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) redl[quad * 4 + h] = l;
       }
-      ok = ok && step_ok;  // a failure here ends the loop at the next barrier
-    }
-    if (ok && n_pg > 0) ok = fold(n_pg - 1);
-    const bool aborted = named_barrier_or(1, 128, !ok || *s_abort != 0);
-    // ---- l over the tokens, normalised partial output (thread = channel) ----------
+      named_barrier_sync(nb, 128);
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      float l = l_run[h];
+      for (int h = 0; h < 4; ++h) L[h] = aborted ? 0.f : redl[h] + redl[4 + h] + redl[8 + h] + redl[12 + h];
+      // ---- merge the two sets' states: set 1 hands over, set 0 writes ---------------------
+      const int mb = k & 1, mph = (k >> 1) & 1;
+      float* mo = reinterpret_cast<float*>(smem + kOffMerge + mb * kMergeBytes);  // o [4][128], m [4], L [4]
+      if (set == 1) {
+        if (warp_wait(bar(kMergeEmpty + mb), mph ^ 1, s_abort)) {
 #pragma unroll
-      for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      if (lane == 0) s_redl[quad * 4 + h] = l;
-    }
-    named_barrier_sync(1, 128);
-    const size_t row0 = ((size_t)j * p.n_splits + split) * kQHeads + kvh * kGqa;
+          for (int h = 0; h < 4; ++h) mo[h * 128 + row] = o_run[h];
+          if (row == 0) {
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const float L = s_redl[h] + s_redl[4 + h] + s_redl[8 + h] + s_redl[12 + h];
-      const bool nonempty = !aborted && L > 0.f && m_run[h] != -INFINITY;
-      p.o_part[(row0 + h) * kHeadDim + row] = nonempty ? o_run[h] / L * p.out_scale : 0.f;
-      if (row == 0) p.lse_part[row0 + h] = nonempty ? (m_run[h] + log2f(L)) * kLn2 : -INFINITY;
+            for (int h = 0; h < 4; ++h) {
+              mo[512 + h] = m_run[h];
+              mo[516 + h] = L[h];
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kMergeFull + mb));
+        }
+      } else {
+        const bool got = warp_wait(bar(kMergeFull + mb), mph, s_abort);
+        const size_t row0 = ((size_t)r->j * p.n_splits + r->split) * kQHeads + r->kvh * kGqa;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float m1 = got ? mo[512 + h] : -INFINITY, L1 = got ? mo[516 + h] : 0.f;
+          const float o1 = got ? mo[h * 128 + row] : 0.f;
+          const float m = fmaxf(m_run[h], m1);
+          const float w0 = (m_run[h] == -INFINITY || L[h] == 0.f) ? 0.f : fast_exp2(m_run[h] - m);
+          const float w1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : fast_exp2(m1 - m);
+          const float Lm = L[h] * w0 + L1 * w1;
+          const bool nonempty = !aborted && got && Lm > 0.f;
+          p.o_part[(row0 + h) * kHeadDim + row] = nonempty ? (o_run[h] * w0 + o1 * w1) / Lm * p.out_scale : 0.f;
+          if (row == 0) p.lse_part[row0 + h] = nonempty ? (m + log2f(Lm)) * kLn2 : -INFINITY;
+        }
+        __syncwarp();
+        if (lane == 0 && got) mbar_arrive(bar(kMergeEmpty + mb));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kRecEmpty + slot));
+      e0 += n;
+      ok = !aborted;
     }
   }
 
-  // ---- teardown -----------------------------------------------------------------------
+  // ---- teardown -------------------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
-  if (*s_abort && tid == 0) {
-    set_status(p.status, MSA_STATUS_TIMEOUT);
-    // bounded drain of the copies that may still be landing: the last two issued
-    // (each earlier one was consumed before its stage was refilled)
+  if (tid == 0) {
+    // every tcgen05.mma is done (both issuers committed after their last one)
     volatile int ignore = 0;
-    const int n_iss = *s_issued;
-    for (int e = max(0, n_iss - 2); e < n_iss; ++e)
-      mbar_wait(bar(kRawFull + (e & 1)), (e >> 1) & 1, &ignore);
+    mbar_wait(bar(kDone), 0, &ignore);
+    mbar_wait(bar(kDone + 1), 0, &ignore);
+    if (*s_abort) {
+      set_status(p.status, MSA_STATUS_TIMEOUT);
+      // bounded drain of the copies that may still be landing: the last kStages
+      // issued on each ring (every earlier one was consumed before its stage was
+      // refilled)
+      const int nk = *s_issued_k, nv = *s_issued_v;
+      for (int e = max(0, nk - kStages); e < nk; ++e)
+        mbar_wait(bar(kKrFull + e % kStages), (e / kStages) & 1, &ignore);
+      for (int e = max(0, nv - kStages); e < nv; ++e)
+        mbar_wait(bar(kVrFull + e % kStages), (e / kStages) & 1, &ignore);
+    }
   }
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -452,22 +627,27 @@ cudaError_t launch_sparse_attn_tc(const msa_cache* c, const uint8_t* q, float so
                                   int n_seqs, int n_q_total, int n_splits, float* o_part,
                                   float* lse_part, cudaStream_t stream) {
   if (n_q_total == 0) return cudaSuccess;
-  static bool s_attr[64] = {false};
+  static int s_n_sm[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!s_attr[dev]) {
-    e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  if (s_n_sm[dev] == 0) {
+    int n_sm = 0;
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    s_attr[dev] = true;
+    e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)attn_smem_bytes(kMaxSeqs));
+    if (e != cudaSuccess) return e;
+    s_n_sm[dev] = n_sm;
   }
+  const int n_items = n_q_total * kKvHeads * n_splits;
   AttnParams ap{static_cast<const uint8_t*>(c->kv_pool), c->n_pages, q, sel, n_sel, block_table,
-                max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, n_splits,
+                max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, n_splits, n_items,
                 softmax_scale / c->s_enc_k * kLog2e, 1.0f / (256.0f * c->s_enc_v), o_part,
                 lse_part, c->status};
-  return launch_pdl(sparse_attn_tc_kernel, dim3(n_splits, kKvHeads, n_q_total), dim3(kThreads),
-                    (size_t)kSmemAlloc, stream, ap);
+  const int grid = n_items < s_n_sm[dev] ? n_items : s_n_sm[dev];
+  return launch_pdl(sparse_attn_tc_kernel, dim3(grid), dim3(kThreads), attn_smem_bytes(n_seqs), stream, ap);
 }
 
 }  // namespace msa

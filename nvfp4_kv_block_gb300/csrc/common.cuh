@@ -127,25 +127,35 @@ __device__ __forceinline__ void build_dequant_table(uint2* tab, int tid, int nth
 
 // Eight E2M1 codes (nibble k = element k) -> eight FP8 operand bytes
 // (x: elements 0..3, y: elements 4..7), each sign(code) | table[|code|].
+// Magnitudes: byte permutes of the scaled table by the 3-bit codes.  Signs:
+// element k's sign is bit 3 of nibble k; for even k that is bit 7 of byte k/2
+// of (w << 4), for odd k bit 7 of byte k/2 of w, so one more byte permute per
+// four elements places every sign bit at bit 7 of its output byte.  9 integer
+// instructions per 8 elements.
 __device__ __forceinline__ uint2 dequant8(uint32_t w, uint2 t) {
   const uint32_t m = w & 0x77777777u;
   const uint32_t mag0 = prmt(t.x, t.y, m);
   const uint32_t mag1 = prmt(t.x, t.y, m >> 16);
-  // selector nibble 8|sign: picks byte 0 (0x00) or byte 1 (0x80) of 0x8000 and
-  // replicates its sign bit -> 0x00 / 0xFF per output byte
-  const uint32_t ssel = ((w >> 3) & 0x11111111u) | 0x88888888u;
-  const uint32_t s0 = prmt(0x8000u, 0u, ssel);
-  const uint32_t s1 = prmt(0x8000u, 0u, ssel >> 16);
+  const uint32_t w4 = w << 4;
+  const uint32_t s0 = prmt(w4, w, 0x5140u);  // bytes: w4.b0, w.b0, w4.b1, w.b1
+  const uint32_t s1 = prmt(w4, w, 0x7362u);  // bytes: w4.b2, w.b2, w4.b3, w.b3
   return make_uint2(mag0 | (s0 & 0x80808080u), mag1 | (s1 & 0x80808080u));
 }
 
 // ---- mbarrier / TMA bulk copy / tcgen05 (inline PTX) --------------------------
-// Every wait is bounded: after kSpinLimit polls the caller gets false and must
-// abandon its loop (the kernel then reports MSA_STATUS_TIMEOUT).
+// Every wait is bounded: after kSpinLimit polls or kWaitLimitNs nanoseconds the
+// caller gets false and must abandon its loop (the kernel then reports
+// MSA_STATUS_TIMEOUT).
 constexpr uint32_t kSpinLimit = 1u << 25;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
@@ -157,10 +167,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// One poll.  The suspend-time hint (20 us) lets the hardware park the thread
+// until the phase completes instead of re-issuing the poll.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -170,9 +182,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits for the phase with the given parity; false on timeout or when another
 // role has already flagged *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 255 && *abort) return false;
+    if ((i & 15) == 0 && (*abort || globaltimer_ns() - t0 > kWaitLimitNs)) break;
   }
   *abort = 1;
   return false;
@@ -279,6 +293,24 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 8 registers per thread -> 32 TMEM lanes x 8 columns (thread = lane).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// D (TMEM) = A (TMEM: row m in lane m, K packed four 8-bit elements per column)
+// x B (shared-memory descriptor), kind::f8f6f4.
+__device__ __forceinline__ void umma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {

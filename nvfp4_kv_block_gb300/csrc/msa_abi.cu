@@ -114,7 +114,7 @@ int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q
   if (n_splits < 1 || n_splits > msa::kMaxSplits || n_q_total < 0 || n_seqs < 0 ||
       max_pages <= 0 || !(softmax_scale > 0.f) || !isfinite(softmax_scale))
     return MSA_ERR_INVALID_ARG;
-  if (n_q_total > 65535) return MSA_ERR_UNSUPPORTED_SHAPE;  // grid.z
+  if (n_q_total > 65535 || n_seqs > msa::kMaxSeqs) return MSA_ERR_UNSUPPORTED_SHAPE;
   if (n_q_total > 0 && (!q || !sel || !n_sel || !block_table || !seq_lens || !q_start_loc ||
                         !o_part || !lse_part || n_seqs == 0))
     return MSA_ERR_INVALID_ARG;

@@ -266,20 +266,21 @@ def debug_fp8_page(cache, page):
     return k8, v8
 
 
-def choose_splits(n_q_total, n_sms=152, ctas_per_sm=3):
+def choose_splits(n_q_total, n_sms=152):
     """Splits per query token for the attention kernel.
 
-    Each (token, KV head, split) CTA processes ceil(17 / splits) pages one after
-    another; with ``ctas_per_sm`` CTAs resident per SM the step takes about
-    waves x pages-per-CTA page times.  Pick the split count that minimises that
-    makespan, preferring fewer splits (less partial-output traffic) on ties.
+    The attention kernel runs one persistent CTA per SM; work items are
+    (token, KV head, split), dealt round-robin, each with up to
+    ceil(17 / splits) pages.  The busiest CTA then streams about
+    ceil(items / SMs) x (pages per item + an item overhead of about two pages);
+    pick the split count that minimises that, with a small charge per split
+    for the partial outputs written and merged, preferring fewer splits on ties.
     """
-    slots = n_sms * ctas_per_sm
     best, best_cost = 1, None
     for s in range(1, TOPK + 2):
-        ctas = KV_HEADS * max(1, n_q_total) * s
-        cost = math.ceil(ctas / slots) * math.ceil((TOPK + 1) / s)
-        cost *= 1.0 + 0.02 * s  # partial outputs written and merged per split
+        items = KV_HEADS * max(1, n_q_total) * s
+        cost = math.ceil(items / n_sms) * (math.ceil((TOPK + 1) / s) + 2.0)
+        cost *= 1.0 + 0.02 * s
         if best_cost is None or cost < best_cost - 1e-9:
             best, best_cost = s, cost
     return best
