@@ -45,6 +45,7 @@ namespace {
 constexpr int kThreads = 640;  // 20 warps
 constexpr int kStages = 6;     // raw K and raw V ring depth
 constexpr int kRecs = 4;       // item records in flight
+constexpr int kK8Slots = 3;    // K8 buffers in tensor memory
 constexpr int kV8Tiles = 3;
 constexpr int kPO = 4;         // P tiles and O buffers
 constexpr int kHalfBytes = kHeadBytes / 2;  // 9,216: codes + scales of K (or V)
@@ -61,8 +62,8 @@ constexpr int kMergeBytes = (4 * 128 + 8) * 4;
 constexpr int kOffBars = kOffMerge + 2 * kMergeBytes;
 // barrier indices
 constexpr int kKrFull = 0, kKrEmpty = kStages, kVrFull = 2 * kStages, kVrEmpty = 3 * kStages;
-constexpr int kK8Full = 4 * kStages, kK8Empty = kK8Full + 2, kSFull = kK8Full + 4,
-              kSEmpty = kK8Full + 6, kV8Full = kK8Full + 8, kV8Empty = kV8Full + kV8Tiles,
+constexpr int kK8Full = 4 * kStages, kK8Empty = kK8Full + kK8Slots, kSFull = kK8Empty + kK8Slots,
+              kSEmpty = kSFull + 2, kV8Full = kSEmpty + 2, kV8Empty = kV8Full + kV8Tiles,
               kPFull = kV8Empty + kV8Tiles, kPEmpty = kPFull + kPO, kOFull = kPEmpty + kPO,
               kOEmpty = kOFull + kPO, kRecFull = kOEmpty + kPO, kRecEmpty = kRecFull + kRecs,
               kMergeFull = kRecEmpty + kRecs, kMergeEmpty = kMergeFull + 2, kDone = kMergeEmpty + 2,
@@ -71,7 +72,10 @@ constexpr int kOffMisc = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;  // tmem, a
 constexpr int kOffRed = kOffMisc + 16;        // float [2 sets][2][4 warps][4 heads] page maxima
 constexpr int kOffRedL = kOffRed + 256;       // float [2 sets][4 warps][4 heads] row sums
 constexpr int kOffQsl = kOffRedL + 128;       // int [n_seqs + 1] copy of q_start_loc
-constexpr uint32_t kTmemCols = 256;           // K8: 0, 32; S: 64, 80; O: 96 + 16 i
+constexpr uint32_t kTmS = 32 * kK8Slots;      // TMEM columns: K8 slot i at 32 i, S slots at kTmS,
+constexpr uint32_t kTmO = kTmS + 32;          // kTmS + 16, O buffers at kTmO + 16 i
+constexpr uint32_t kTmemCols = 256;
+static_assert(kTmO + 16 * kPO <= kTmemCols, "tensor memory columns");
 constexpr int kRecEmptyCount = 1 + 4 + 4 + 1 + 1 + 8;  // producer, K, V, QK, PV, softmax
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -171,9 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       mbar_init(bar(kVrFull + i), 1);
       mbar_init(bar(kVrEmpty + i), 4);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kK8Slots; ++i) {
       mbar_init(bar(kK8Full + i), 4);
       mbar_init(bar(kK8Empty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSFull + i), 1);
       mbar_init(bar(kSEmpty + i), 4);
       mbar_init(bar(kMergeFull + i), 4);
@@ -318,16 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const int n = rec(slot)->n_pg;
         const uint64_t bdesc = umma_desc_sw128(sbase + kOffQ + slot * 2048);
         for (int i = 0; i < n; ++i, ++e) {
-          const int sl = e & 1, ph = (e >> 1) & 1;
-          if (!mbar_wait(bar(kK8Full + sl), ph, s_abort) || !mbar_wait(bar(kSEmpty + sl), ph ^ 1, s_abort)) {
+          const int sl = e & 1, ph = (e >> 1) & 1, ks = e % kK8Slots, kph = (e / kK8Slots) & 1;
+          if (!mbar_wait(bar(kK8Full + ks), kph, s_abort) || !mbar_wait(bar(kSEmpty + sl), ph ^ 1, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // K = 32 per MMA: 8 TMEM columns of A, +32 B (+2) of B
-            umma_e4m3_ts(tmem + 64 + 16 * sl, tmem + 32 * sl + 8 * kk, bdesc + 2 * kk, idesc, kk > 0);
-          umma_commit(bar(kK8Empty + sl));
+            umma_e4m3_ts(tmem + kTmS + 16 * sl, tmem + 32 * ks + 8 * kk, bdesc + 2 * kk, idesc, kk > 0);
+          umma_commit(bar(kK8Empty + ks));
           umma_commit(bar(kSFull + sl));
         }
         if (!ok) break;
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
             // A: V tile read MN-major; 32 tokens (4 swizzle atoms of 8 rows) per MMA
             const uint64_t adesc =
                 umma_desc_sw128_lbo_sbo(sbase + kOffV8 + v * kTileBytes + kk * 4096, 1024, 1024);
-            umma_e4m3(tmem + 96 + 16 * po, adesc, bdesc + 2 * kk, idesc, kk > 0);
+            umma_e4m3(tmem + kTmO + 16 * po, adesc, bdesc + 2 * kk, idesc, kk > 0);
           }
           umma_commit(bar(kV8Empty + v));
           umma_commit(bar(kPEmpty + po));
@@ -389,9 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       const int n = r->n_pg;
       for (int i = 0; i < n; ++i, ++e) {
         const int st = e % kStages;
-        // output slot: K8 buffer e % 2 (freed by QK(e-2)), V8 tile e % 3 (freed by PV(e-3))
-        const int os = is_k ? (e & 1) : e % kV8Tiles;
-        const int oph = is_k ? ((e >> 1) & 1) : ((e / kV8Tiles) & 1);
+        // output slot: K8 buffer e % kK8Slots (freed by its previous QK), V8 tile
+        // e % kV8Tiles (freed by its previous PV)
+        const int os = is_k ? e % kK8Slots : e % kV8Tiles;
+        const int oph = is_k ? ((e / kK8Slots) & 1) : ((e / kV8Tiles) & 1);
         if (!warp_wait(bar(full0 + st), (e / kStages) & 1, s_abort) ||
             !warp_wait(bar((is_k ? kK8Empty : kV8Empty) + os), oph ^ 1, s_abort)) {
           ok = false;
@@ -460,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         if (!warp_wait(bar(kOFull + po), (ef >> 2) & 1, s_abort)) return false;
         tc_fence_after();
         float ov[8];
-        tmem_ld8(trow + 96 + 16 * po, ov);  // columns 0-3: hi terms, 4-7: remainders
+        tmem_ld8(trow + kTmO + 16 * po, ov);  // columns 0-3: hi terms, 4-7: remainders
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kOEmpty + po));
@@ -475,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         float sv[4] = {0.f, 0.f, 0.f, 0.f};
         if (good) {
           tc_fence_after();
-          tmem_ld4(trow + 64 + 16 * set, sv);
+          tmem_ld4(trow + kTmS + 16 * set, sv);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kSEmpty + set));

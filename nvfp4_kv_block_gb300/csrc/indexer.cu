@@ -63,7 +63,17 @@ constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccs + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffPrefix = kOffMisc + 16;
 
-size_t scan_smem_bytes(int n_seqs) { return 1024 + kOffPrefix + 4 * (size_t)(n_seqs + 1); }
+// After kOffPrefix, per sequence: weighted page prefix (int64, n_seqs + 1),
+// page prefix (n_seqs + 1), seq_lens (n_seqs), q_start_loc (n_seqs + 1).
+size_t scan_smem_bytes(int n_seqs) { return 1024 + kOffPrefix + 20 * (size_t)n_seqs + 16; }
+
+// Relative cost of scanning one page for a sequence with n_q query tokens: a
+// fixed part per pass of up to 8 tokens (the page's bytes) plus the epilogue's
+// per-token part (measured: a pass with 8 tokens costs about 1.3x one with 1).
+constexpr int kPassCost = 23;
+__device__ __forceinline__ long long page_weight(int n_q) {
+  return (long long)((n_q + kNqMax - 1) / kNqMax) * kPassCost + n_q;
+}
 
 // Pages to scan for sequence b: blocks 0..r_last-1, r_last = (seq_len-1)/128.
 __device__ __forceinline__ int scan_pages(const SeqInfo& s) {
@@ -73,8 +83,8 @@ __device__ __forceinline__ int scan_pages(const SeqInfo& s) {
 // Walks the segments (sequence, query-token group, page range) of the flattened
 // page range [pg, pg_end).  Every role of the CTA walks the same sequence.
 template <typename F>
-__device__ __forceinline__ void for_each_segment(const ScanParams& p, const int* s_prefix, long long pg,
-                                                 long long pg_end, F&& f) {
+__device__ __forceinline__ void for_each_segment(const ScanParams& p, const int* s_prefix, const int* s_sl,
+                                                 const int* s_qsl, long long pg, long long pg_end, F&& f) {
   int lo = 0, hi = p.n_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -83,7 +93,7 @@ __device__ __forceinline__ void for_each_segment(const ScanParams& p, const int*
   int b = lo;
   while (pg < pg_end) {
     while (s_prefix[b + 1] <= pg) ++b;
-    const SeqInfo s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
+    const SeqInfo s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
     const int page0 = (int)(pg - s_prefix[b]);
     const int page1 = (int)(min((long long)s_prefix[b + 1], pg_end) - s_prefix[b]);
     for (int j0 = 0; j0 < s.n_q; j0 += kNqMax) {
@@ -114,28 +124,30 @@ struct TopkSmem {
   unsigned long long* cand;  // [kMaxCand]
   unsigned long long* tmax;  // [NT] half-warp maxima / reduction scratch
   int* win;                  // [16]
-  int* misc;                 // [0] n_cand, [1] sequence
+  int* misc;                 // [0] n_cand
 };
 
 // Sequence of query token j (-1 if none): the b with q_start_loc[b] <= j <
-// q_start_loc[b+1], found by all NT threads in one pass.
-template <int NT>
-__device__ int token_sequence(const ScanParams& p, int j, int* slot) {
-  if (threadIdx.x == 0) *slot = -1;
-  __syncthreads();
-  for (int base = 0; base < p.n_seqs; base += NT) {
-    const int b = base + threadIdx.x;
-    if (b < p.n_seqs && p.q_start_loc[b] <= j && j < p.q_start_loc[b + 1]) *slot = b;
+// q_start_loc[b+1], by binary search in the shared-memory copy of q_start_loc
+// (non-decreasing for valid input; anything else ends as -1 or a sequence that
+// fails its checks).
+__device__ __forceinline__ int token_sequence(const int* s_qsl, int n_seqs, int j) {
+  if (n_seqs <= 0) return -1;
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_qsl[mid] <= j) lo = mid; else hi = mid - 1;
   }
-  __syncthreads();
-  return *slot;
+  return (s_qsl[lo] <= j && j < s_qsl[lo + 1]) ? lo : -1;
 }
 
 template <int NT>
-__device__ void select_token(const ScanParams& p, int j, int b, const TopkSmem& sm) {
+__device__ void select_token(const ScanParams& p, int j, const int* s_sl, const int* s_qsl,
+                             const TopkSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31;
+  const int b = token_sequence(s_qsl, p.n_seqs, j);
   SeqInfo s{0, 0, 0, false};
-  if (b >= 0) s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
+  if (b >= 0) s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
   int* out = p.sel + (size_t)j * kSelStride;
   if (b < 0 || !s.ok) {
     if (tid == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
@@ -188,20 +200,32 @@ __device__ void select_token(const ScanParams& p, int j, int b, const TopkSmem& 
 #pragma unroll 4
     for (int i = 1; i < NT / 16; ++i) theta = sm.tmax[i] < theta ? sm.tmax[i] : theta;
   }
-  for (int blk = tid; blk < r; blk += NT) {
-    const unsigned long long k = key(blk);
-    if (k >= theta) {
-      const int slot = atomicAdd(&sm.misc[0], 1);
-      if (slot < kMaxCand) sm.cand[slot] = k;
-    }
+  // candidates: keys >= theta, appended with one shared-memory atomic per warp
+  for (int base = 0; base < r; base += NT) {
+    const int blk = base + tid;
+    const unsigned long long k = blk < r ? key(blk) : 0ull;
+    const bool take = blk < r && k >= theta;
+    const unsigned mask = __ballot_sync(0xffffffffu, take);
+    int at = 0;
+    if (lane == 0 && mask) at = atomicAdd(&sm.misc[0], __popc(mask));
+    at = __shfl_sync(0xffffffffu, at, 0) + __popc(mask & ((1u << lane) - 1));
+    if (take && at < kMaxCand) sm.cand[at] = k;
   }
   __syncthreads();
   const int nc = sm.misc[0];
   if (nc <= kMaxCand) {
+    // exact rank of each candidate by counting; pairs of keys per load (a zero
+    // pad never counts: every key is > 0)
+    if (tid == 0 && (nc & 1) && nc < kMaxCand) sm.cand[nc] = 0ull;
+    __syncthreads();
+    const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(sm.cand);
     for (int c = tid; c < nc; c += NT) {
       const unsigned long long k = sm.cand[c];
       int rk = 0;
-      for (int i = 0; i < nc; ++i) rk += sm.cand[i] > k;
+      for (int i = 0; i < (nc + 1) / 2; ++i) {
+        const ulonglong2 v = c2[i];
+        rk += (v.x > k) + (v.y > k);
+      }
       if (rk < kTopK) sm.win[rk] = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFu));
     }
   } else {
@@ -240,25 +264,27 @@ __device__ void select_token(const ScanParams& p, int j, int b, const TopkSmem& 
   }
 }
 
-// Grid-wide barrier of a cooperative launch (all CTAs co-resident): arrival
-// counter back to zero at every release, generation word bumped.  Bounded: on
-// timeout it raises *abort and returns false.
+// Grid-wide barrier of a cooperative launch (all CTAs co-resident), used once
+// per launch.  Each CTA fences its writes and counts itself in; the last one
+// bumps the generation word (releasing the others at once) and then returns
+// the counter to zero for the next launch.  Bounded: on timeout it raises
+// *abort and returns false.
 __device__ bool grid_barrier(unsigned int* sync, unsigned int n_ctas, volatile int* abort) {
   __threadfence();
   volatile unsigned int* gen = sync + 1;
   const unsigned int g = *gen;
   if (atomicAdd(sync, 1u) == n_ctas - 1) {
-    atomicExch(sync, 0u);
-    __threadfence();
     atomicAdd(sync + 1, 1u);
+    atomicExch(sync, 0u);
     return true;
   }
-  for (uint32_t i = 0; i < (kSpinLimit >> 4); ++i) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (*gen != g) {
       __threadfence();
       return true;
     }
-    __nanosleep(64);
+    if ((i & 63) == 63 && globaltimer_ns() - t0 > kWaitLimitNs) break;
   }
   *abort = 1;
   return false;
@@ -279,56 +305,83 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   const uint32_t done_bar = bar0 + 8 * (2 * kStages + 4 + 2 * kAccs);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int* s_prefix = reinterpret_cast<int*>(smem + kOffPrefix);
+  long long* s_wpre = reinterpret_cast<long long*>(smem + kOffPrefix);
+  int* s_prefix = reinterpret_cast<int*>(s_wpre + (p.n_seqs + 1));
+  int* s_sl = s_prefix + (p.n_seqs + 1);
+  int* s_qsl = s_sl + p.n_seqs;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();     // inputs may come from the previous kernel in the stream
   pdl_trigger();  // the attention kernel may launch and run its prologue
 
-  // -- exclusive prefix over sequences of the pages each one scans ------------
-  {
-    const int per = (p.n_seqs + kScanThreads - 1) / kScanThreads;
-    const int b0 = tid * per;
-    int local = 0;
-    for (int b = b0; b < b0 + per && b < p.n_seqs; ++b) {
-      const SeqInfo s = load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total);
-      if (!s.ok && blockIdx.x == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
-      local += scan_pages(s);
+  // -- sequence metadata in shared memory; exclusive prefixes over sequences of
+  //    the pages each one scans and of their weighted cost ----------------------
+  for (int b = tid; b <= p.n_seqs; b += kScanThreads) s_qsl[b] = p.q_start_loc[b];
+  for (int b = tid; b < p.n_seqs; b += kScanThreads) s_sl[b] = p.seq_lens[b];
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), 1);
     }
-    int incl = local;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bfull(i), 1);
+      mbar_init(bempty(i), 1);
+    }
+    for (int i = 0; i < kAccs; ++i) {
+      mbar_init(tfull(i), 1);
+      mbar_init(tempty(i), 4);
+    }
+    mbar_init(done_bar, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  {
+    // thread t takes the contiguous run of sequences [b0, b0 + per)
+    const int per = (p.n_seqs + kScanThreads - 1) / kScanThreads;
+    const int b0 = tid * per, b1 = min(b0 + per, p.n_seqs);
+    long long lp = 0, lw = 0;
+    for (int b = b0; b < b1; ++b) {
+      const SeqInfo s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
+      if (!s.ok && blockIdx.x == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
+      const int pages = scan_pages(s);
+      lp += pages;
+      lw += pages * page_weight(s.n_q);
+    }
+    // block-wide exclusive scan of (lp, lw): warp scans, then the warp totals
+    long long ip = lp, iw = lw;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+      const long long yp = __shfl_up_sync(0xffffffffu, ip, o);
+      const long long yw = __shfl_up_sync(0xffffffffu, iw, o);
+      if (lane >= o) {
+        ip += yp;
+        iw += yw;
+      }
     }
-    __shared__ int s_warp_sum[kScanThreads / 32];
-    if (lane == 31) s_warp_sum[warp] = incl;
-    if (tid == 0) {
-      for (int i = 0; i < kStages; ++i) {
-        mbar_init(full(i), 1);
-        mbar_init(empty(i), 1);
-      }
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(bfull(i), 1);
-        mbar_init(bempty(i), 1);
-      }
-      for (int i = 0; i < kAccs; ++i) {
-        mbar_init(tfull(i), 1);
-        mbar_init(tempty(i), 4);
-      }
-      mbar_init(done_bar, 1);
-      *s_abort = 0;
-      fence_barrier_init();
+    __shared__ long long s_wsum[2][kScanThreads / 32];
+    if (lane == 31) {
+      s_wsum[0][warp] = ip;
+      s_wsum[1][warp] = iw;
     }
     __syncthreads();
-    int base = 0;
-    for (int i = 0; i < warp; ++i) base += s_warp_sum[i];
-    int run = base + incl - local;
-    for (int b = b0; b < b0 + per && b < p.n_seqs; ++b) {
-      s_prefix[b] = run;
-      run += scan_pages(load_seq(b, p.seq_lens, p.q_start_loc, p.max_pages, p.n_q_total));
+    long long rp = ip - lp, rw = iw - lw;
+    for (int i = 0; i < warp; ++i) {
+      rp += s_wsum[0][i];
+      rw += s_wsum[1][i];
     }
-    if (tid == kScanThreads - 1) s_prefix[p.n_seqs] = base + incl;
+    for (int b = b0; b < b1; ++b) {
+      s_prefix[b] = (int)rp;
+      s_wpre[b] = rw;
+      const SeqInfo s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
+      const int pages = scan_pages(s);
+      rp += pages;
+      rw += pages * page_weight(s.n_q);
+    }
+    if (tid == kScanThreads - 1) {
+      s_prefix[p.n_seqs] = (int)rp;
+      s_wpre[p.n_seqs] = rw;
+    }
   }
   if (warp == 1) tmem_alloc(smem_u32(s_tmem), kTmemCols);
   tc_fence_before();
@@ -336,14 +389,25 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  const long long total = s_prefix[p.n_seqs];
-  const long long pg_begin = (long long)blockIdx.x * total / gridDim.x;
-  const long long pg_end = (long long)(blockIdx.x + 1) * total / gridDim.x;
+  // CTA c scans the pages whose weighted cost falls in [c W / G, (c+1) W / G)
+  const long long w_total = s_wpre[p.n_seqs];
+  auto page_at = [&](long long x) -> long long {
+    if (x >= w_total) return s_prefix[p.n_seqs];
+    int lo = 0, hi = p.n_seqs - 1;  // last b with s_wpre[b] <= x: a sequence with pages
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_wpre[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const SeqInfo s = load_seq(lo, s_sl, s_qsl, p.max_pages, p.n_q_total);
+    return s_prefix[lo] + (x - s_wpre[lo]) / page_weight(s.n_q);
+  };
+  const long long pg_begin = page_at((long long)blockIdx.x * w_total / gridDim.x);
+  const long long pg_end = page_at((long long)(blockIdx.x + 1) * w_total / gridDim.x);
 
   if (warp == 0) {
     // ---------------- producer: index pages -----------------------------------
     int it = 0;
-    for_each_segment(p, s_prefix, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
+    for_each_segment(p, s_prefix, s_sl, s_qsl, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
       // block-table entries are fetched 32 at a time (one coalesced load per
       // 32 pages, the next batch in flight) so that no dependent global load
       // sits between two page copies
@@ -375,7 +439,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   } else if (warp == 1) {
     // ---------------- MMA warp: B tile of each segment, then the MMAs ----------
     int it = 0, sg = 0;
-    for_each_segment(p, s_prefix, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
+    for_each_segment(p, s_prefix, s_sl, s_qsl, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
       const int slot = sg & 1;
       // the MMAs that read this slot two segments ago must be done
       if (!mbar_wait(bempty(slot), ((sg >> 1) & 1) ^ 1, s_abort)) return false;
@@ -437,7 +501,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
     // max over its 32 token rows, the top-k phase takes the max of the four.
     const int quad = warp & 3, set = (warp - 2) >> 2;
     int it = 0;
-    for_each_segment(p, s_prefix, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
+    for_each_segment(p, s_prefix, s_sl, s_qsl, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
       float wr[kNqMax][kIdxHeads];
 #pragma unroll
       for (int jj = 0; jj < kNqMax; ++jj)
@@ -509,14 +573,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   sm.tmax = reinterpret_cast<unsigned long long*>(smem + kOffB);                       // NT x 8 B
   sm.win = reinterpret_cast<int*>(smem + kOffB + 8 * kScanThreads);
   sm.misc = sm.win + kTopK;
-  // the first token's sequence is looked up while other CTAs finish scanning
-  int b_first = blockIdx.x < p.n_q_total ? token_sequence<kScanThreads>(p, blockIdx.x, sm.misc + 1) : -1;
   if (tid == 0 && !*s_abort) grid_barrier(p.sync, gridDim.x, s_abort);
   __syncthreads();
   if (!*s_abort) {
     for (int j = blockIdx.x; j < p.n_q_total; j += gridDim.x) {
-      const int b = j == (int)blockIdx.x ? b_first : token_sequence<kScanThreads>(p, j, sm.misc + 1);
-      select_token<kScanThreads>(p, j, b, sm);
+      select_token<kScanThreads>(p, j, s_sl, s_qsl, sm);
       __syncthreads();
     }
   }
