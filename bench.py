@@ -1,8 +1,8 @@
 """Benchmark of the NVFP4 block-sparse attention decode step on GB300.
 
 One step = indexer (block scores + top-16/recent selection, one cooperative
-launch) + split sparse attention + LSE merge (the decode path's three kernels)
-over one batch of resident query tokens.  Prints ONE JSON line (rank 0).
+launch) + split sparse attention + LSE merge of the splits (skipped when there
+is one split: its output is final) over one batch of resident query tokens.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl gb300|reference]
 
@@ -153,7 +153,8 @@ def run_gpu(args, rank, world, local_rank):
     n_sel = bufs.n_sel.cpu().numpy()
     idx_bytes, kv_bytes, alg_bytes = algorithmic_bytes(wl, sel, n_sel)
 
-    # the step as one CUDA graph (scan, top-k, attention, merge: chained with
+    # the step as one CUDA graph (indexer, attention and, with several splits, the
+    # merge: chained with
     # programmatic dependent launch) so that host launch latency does not gap
     # the kernels; a second graph holds the indexer alone for its own timing
     def run_indexer():
@@ -163,7 +164,8 @@ def run_gpu(args, rank, world, local_rank):
     def run_attention():
         ops.sparse_attn_decode(st.cache, q, bufs.sel, bufs.n_sel, st.block_table, st.seq_lens,
                                st.q_start_loc, n_splits, o_part=bufs.o_part, lse_part=bufs.lse_part)
-        ops.merge_splits(bufs.o_part, bufs.lse_part, out=bufs.out)
+        if n_splits > 1:  # a single split's output is final
+            ops.merge_splits(bufs.o_part, bufs.lse_part, out=bufs.out)
 
     def run_step():
         run_indexer()
@@ -249,7 +251,7 @@ def run_gpu(args, rank, world, local_rank):
         ms, t_idx, e2e = (float(x) for x in t.cpu())
     return dict(wl=wl, T=T, ms=ms, t_idx=t_idx, e2e=e2e, h2d=h2d, d2h=d2h, n_splits=n_splits,
                 idx_bytes=idx_bytes, kv_bytes=kv_bytes, alg_bytes=alg_bytes, clocks=clk,
-                launches=3 * args.steps)
+                launches=(3 if n_splits > 1 else 2) * args.steps)
 
 
 def oracle_sample(wl, device, budget_s):

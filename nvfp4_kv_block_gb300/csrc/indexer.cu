@@ -61,7 +61,7 @@ constexpr int kOffB = kStages * kIdxPageBytes;  // 131,072
 constexpr int kOffBars = kOffB + 2 * kBBytes;   // 147,456
 constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccs + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kOffPrefix = kOffMisc + 16;
+constexpr int kOffPrefix = kOffMisc + 32;  // misc: tmem slot, abort, page range [2] (int64)
 
 // After kOffPrefix, per sequence: weighted page prefix (int64, n_seqs + 1),
 // page prefix (n_seqs + 1), seq_lens (n_seqs), q_start_loc (n_seqs + 1).
@@ -401,8 +401,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
     const SeqInfo s = load_seq(lo, s_sl, s_qsl, p.max_pages, p.n_q_total);
     return s_prefix[lo] + (x - s_wpre[lo]) / page_weight(s.n_q);
   };
-  const long long pg_begin = page_at((long long)blockIdx.x * w_total / gridDim.x);
-  const long long pg_end = page_at((long long)(blockIdx.x + 1) * w_total / gridDim.x);
+  // one thread computes the range (64-bit divisions are slow in every thread)
+  long long* s_range = reinterpret_cast<long long*>(smem + kOffMisc + 8);
+  if (tid == 0) {
+    s_range[0] = page_at((long long)blockIdx.x * w_total / gridDim.x);
+    s_range[1] = page_at((long long)(blockIdx.x + 1) * w_total / gridDim.x);
+  }
+  __syncthreads();
+  const long long pg_begin = s_range[0], pg_end = s_range[1];
 
   if (warp == 0) {
     // ---------------- producer: index pages -----------------------------------

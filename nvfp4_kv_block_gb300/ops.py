@@ -296,14 +296,18 @@ class DecodeBuffers:
         self.n_sel = torch.empty((n_q_total,), dtype=torch.int32, device=device)
         self.o_part = torch.empty((n_q_total, n_splits, Q_HEADS, HEAD_DIM), dtype=torch.float32, device=device)
         self.lse_part = torch.empty((n_q_total, n_splits, Q_HEADS), dtype=torch.float32, device=device)
-        self.out = torch.empty((n_q_total, Q_HEADS, HEAD_DIM), dtype=torch.float32, device=device)
+        # one split: its normalised output is already the answer (no merge launch)
+        self.out = (self.o_part.view(n_q_total, Q_HEADS, HEAD_DIM) if n_splits == 1 else
+                    torch.empty((n_q_total, Q_HEADS, HEAD_DIM), dtype=torch.float32, device=device))
 
 
 def decode_step(cache, q, q_idx, w, block_table, seq_lens, q_start_loc, bufs, softmax_scale=None):
-    """One decode step: indexer top-k, sparse attention splits, LSE merge (3 kernels)."""
+    """One decode step: indexer top-k, sparse attention splits, and the LSE merge
+    of the splits (3 kernels; 2 with a single split, whose output is final)."""
     indexer_topk(cache, q_idx, w, block_table, seq_lens, q_start_loc, ws=bufs.ws, sel=bufs.sel,
                  n_sel=bufs.n_sel)
     sparse_attn_decode(cache, q, bufs.sel, bufs.n_sel, block_table, seq_lens, q_start_loc,
                        bufs.n_splits, softmax_scale, o_part=bufs.o_part, lse_part=bufs.lse_part)
-    merge_splits(bufs.o_part, bufs.lse_part, out=bufs.out)
+    if bufs.n_splits > 1:
+        merge_splits(bufs.o_part, bufs.lse_part, out=bufs.out)
     return bufs.out
