@@ -122,7 +122,7 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
 struct TopkSmem {
   float* sc;                 // [kTopkStage]
   unsigned long long* cand;  // [kMaxCand]
-  unsigned long long* tmax;  // [NT] half-warp maxima / reduction scratch
+  unsigned long long* tmax;  // [NT] per-warp survivors, theta, reduction scratch
   int* win;                  // [16]
   int* misc;                 // [0] n_cand
 };
@@ -176,41 +176,88 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
            (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
   };
   if (staged) {
-#pragma unroll 8
-    for (int blk = tid; blk < r; blk += NT) {
-      const float4 v = __ldcg(row + blk);
-      sm.sc[blk] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    // batches of 8 loads in flight per thread, then the stores
+    for (int base = tid; base < r; base += 8 * NT) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int blk = base + u * NT;
+        v[u] = blk < r ? __ldcg(row + blk) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int blk = base + u * NT;
+        if (blk < r) sm.sc[blk] = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
+      }
     }
   }
   if (tid == 0) sm.misc[0] = 0;
   __syncthreads();
-  // theta: thread t owns blocks t, t + NT, ...; half-warp h owns the blocks with
-  // (blk mod NT) in [16h, 16h+16).  When all NT/16 >= 16 half-warps own a block
-  // (r > NT - 16), their maxima are NT/16 distinct keys whose minimum is <= the
-  // 16th largest key; otherwise theta = 0 and every block is a candidate.
-  unsigned long long theta = 0;
-  if (r > NT - 16) {
-    unsigned long long mykey = 0;
-    for (int blk = tid; blk < r; blk += NT) mykey = umax64(mykey, key(blk));
+  // theta: thread t owns blocks t, t + NT, ...  Each warp sorts its 32 thread
+  // maxima (bitonic, by shuffles), so lane i holds the warp's (i+1)-th largest.
+  // For m in {2, 4, 8, 16}: if 16/m warps each have m keys at or above x, then
+  // x <= the 16th largest key; so the (16/m)-th largest of the warps' m-th
+  // largest maxima is a lower bound of the 16th largest key, and theta is the
+  // largest of these four bounds.  Every winner is then a candidate.  (r > 16
+  // here; real keys are distinct and > 0, a missing key counts as 0.)
+  constexpr int kNW = NT / 32;
+  unsigned long long v = 0;
+  for (int blk = tid; blk < r; blk += NT) v = umax64(v, key(blk));
 #pragma unroll
-    for (int o = 8; o; o >>= 1) mykey = umax64(mykey, __shfl_xor_sync(0xffffffffu, mykey, o));
-    if ((lane & 15) == 0) sm.tmax[tid >> 4] = mykey;
-    __syncthreads();
-    theta = sm.tmax[0];
-#pragma unroll 4
-    for (int i = 1; i < NT / 16; ++i) theta = sm.tmax[i] < theta ? sm.tmax[i] : theta;
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, jj);
+      // descending overall: the lower lane of a pair keeps the larger value in
+      // blocks whose bit k is clear, the smaller one where it is set
+      const bool lower = (lane & jj) == 0, asc = (lane & k) == 0;
+      v = (lower == asc) ? umax64(v, o) : (v < o ? v : o);
+    }
   }
-  // candidates: keys >= theta, appended with one shared-memory atomic per warp
-  for (int base = 0; base < r; base += NT) {
-    const int blk = base + tid;
-    const unsigned long long k = blk < r ? key(blk) : 0ull;
-    const bool take = blk < r && k >= theta;
-    const unsigned mask = __ballot_sync(0xffffffffu, take);
-    int at = 0;
-    if (lane == 0 && mask) at = atomicAdd(&sm.misc[0], __popc(mask));
-    at = __shfl_sync(0xffffffffu, at, 0) + __popc(mask & ((1u << lane) - 1));
-    if (take && at < kMaxCand) sm.cand[at] = k;
+  // tmax[4w + s] = warp w's (2 << s)-th largest maximum; tmax[4 kNW] = theta
+  if (lane == 1 || lane == 3 || lane == 7 || lane == 15)
+    sm.tmax[(tid >> 5) * 4 + (31 - __clz(lane + 1)) - 1] = v;
+  if (tid == 0) sm.tmax[4 * kNW] = 0ull;
+  __syncthreads();
+  if (tid < 4 * kNW) {
+    const int set = tid & 3;
+    const unsigned long long x = sm.tmax[tid];
+    int rk = 0;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) rk += sm.tmax[4 * w + set] > x;
+    if (rk == (8 >> set) - 1) atomicMax(&sm.tmax[4 * kNW], x);
   }
+  __syncthreads();
+  const unsigned long long theta = sm.tmax[4 * kNW];
+  // candidates: keys >= theta, written without atomics: per-thread counts, a
+  // scan over lanes and warps, then each thread writes its own
+  int cnt = 0;
+  for (int blk = tid; blk < r; blk += NT) cnt += key(blk) >= theta;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.misc[1 + (tid >> 5)] = incl;
+  __syncthreads();
+  int at = incl - cnt, nc_all = 0;
+#pragma unroll
+  for (int w = 0; w < kNW; ++w) {
+    const int c = sm.misc[1 + w];
+    at += w < (tid >> 5) ? c : 0;
+    nc_all += c;
+  }
+  if (cnt) {
+    for (int blk = tid; blk < r; blk += NT) {
+      const unsigned long long k = key(blk);
+      if (k >= theta) {
+        if (at < kMaxCand) sm.cand[at] = k;
+        ++at;
+      }
+    }
+  }
+  if (tid == 0) sm.misc[0] = nc_all;
   __syncthreads();
   const int nc = sm.misc[0];
   if (nc <= kMaxCand) {
