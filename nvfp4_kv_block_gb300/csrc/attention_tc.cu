@@ -19,10 +19,10 @@
 //                tile, into a 4-deep ring of item records;
 //   warp 1       TMA producer: per page two 9 KB cp.async.bulk copies, the K
 //                half (codes + scales) and the V half, into two 6-stage rings;
-//   warps 12-15  K conversion, thread = token: NVFP4 -> FP8 through a 256-entry
+//   warps 12-19  K conversion, thread = (token, half row): NVFP4 -> FP8 through a 256-entry
 //                shared table of scaled E4M3 values and byte permutes, written
 //                with tcgen05.st straight into tensor memory (the A operand);
-//   warps 16-19  V conversion, thread = token: the same into a 128-byte-swizzled
+//   warps 20-27  V conversion, thread = (token, half row): the same into a 128-byte-swizzled
 //                shared-memory tile (3 tiles);
 //   warp 2       QK issuer: S = K8 Q^T (kind::f8f6f4, M = 128 tokens, N = 16: the
 //                4 query heads, zero padded, K = 128, A from tensor memory);
@@ -42,7 +42,8 @@
 namespace msa {
 namespace {
 
-constexpr int kThreads = 640;  // 20 warps
+constexpr int kConvSets = 2;   // warps per token row of K (and of V): each converts 4 / kConvSets chunks
+constexpr int kThreads = 32 * (12 + 8 * kConvSets);
 constexpr int kStages = 6;     // raw K and raw V ring depth
 constexpr int kRecs = 4;       // item records in flight
 constexpr int kK8Slots = 3;    // K8 buffers in tensor memory
@@ -76,7 +77,7 @@ constexpr uint32_t kTmS = 32 * kK8Slots;      // TMEM columns: K8 slot i at 32 i
 constexpr uint32_t kTmO = kTmS + 32;          // kTmS + 16, O buffers at kTmO + 16 i
 constexpr uint32_t kTmemCols = 256;
 static_assert(kTmO + 16 * kPO <= kTmemCols, "tensor memory columns");
-constexpr int kRecEmptyCount = 1 + 4 + 4 + 1 + 1 + 8;  // producer, K, V, QK, PV, softmax
+constexpr int kRecEmptyCount = 1 + 8 * kConvSets + 1 + 1 + 8;  // producer, K and V, QK, PV, softmax
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1 KB alignment");
@@ -171,12 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kKrFull + i), 1);
-      mbar_init(bar(kKrEmpty + i), 4);
+      mbar_init(bar(kKrEmpty + i), 4 * kConvSets);
       mbar_init(bar(kVrFull + i), 1);
-      mbar_init(bar(kVrEmpty + i), 4);
+      mbar_init(bar(kVrEmpty + i), 4 * kConvSets);
     }
     for (int i = 0; i < kK8Slots; ++i) {
-      mbar_init(bar(kK8Full + i), 4);
+      mbar_init(bar(kK8Full + i), 4 * kConvSets);
       mbar_init(bar(kK8Empty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       mbar_init(bar(kMergeEmpty + i), 4);
     }
     for (int i = 0; i < kV8Tiles; ++i) {
-      mbar_init(bar(kV8Full + i), 4);
+      mbar_init(bar(kV8Full + i), 4 * kConvSets);
       mbar_init(bar(kV8Empty + i), 1);
     }
     for (int i = 0; i < kPO; ++i) {
@@ -380,8 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
     }
     __syncwarp();
   } else if (warp >= 12) {
-    // ---------------- conversion: K (warps 12-15) or V (warps 16-19), thread = token ----
-    const bool is_k = warp < 16;
+    // ---------------- conversion: K (warps 12 ..) or V (the next 4 kConvSets) --------
+    // thread = token; the kConvSets warps of a token row take its 16-byte code
+    // chunks c = cs * kCh .. cs * kCh + kCh - 1
+    const bool is_k = warp < 12 + 4 * kConvSets;
+    constexpr int kCh = 4 / kConvSets;
+    const int cs = ((warp - 12) >> 2) % kConvSets;
     // K warps write TMEM lanes 32 (warp % 4) ..; V warps any order
     const int tok = 32 * (warp & 3) + lane;
     const int full0 = is_k ? kKrFull : kVrFull, empty0 = is_k ? kKrEmpty : kVrEmpty;
@@ -411,7 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * os;
         uint8_t* dst = smem + kOffV8 + os * kTileBytes + tok * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int ci = 0; ci < kCh; ++ci) {
+          const int c = cs * kCh + ci;
           uint32_t o[8];
           convert_chunk(raw, s_tab, tok, c, live, o);
           if (is_k) {
