@@ -19,36 +19,45 @@
 //                tile, into a 4-deep ring of item records;
 //   warp 1       TMA producer: per page two 9 KB cp.async.bulk copies, the K
 //                half (codes + scales) and the V half, into two 6-stage rings;
-//   warps 12-19  K conversion, thread = (token, half row): NVFP4 -> FP8 through a 256-entry
-//                shared table of scaled E4M3 values and byte permutes, written
-//                with tcgen05.st straight into tensor memory (the A operand);
-//   warps 20-27  V conversion, thread = (token, half row): the same into a 128-byte-swizzled
-//                shared-memory tile (3 tiles);
 //   warp 2       QK issuer: S = K8 Q^T (kind::f8f6f4, M = 128 tokens, N = 16: the
 //                4 query heads, zero padded, K = 128, A from tensor memory);
 //   warp 3       PV issuer: O^T = V8^T P (A = the V tile read MN-major, no
-//                transpose, B = P), one of 4 TMEM O buffers per page;
-//   warps 4-11   softmax, two sets of 4 warps; set s takes the pages with
-//                e % 2 == s and keeps its own running (m, l, o): thread = token
+//                transpose, B = P), one of 4 TMEM O buffers per page; its one
+//                commit per page completes the page's O barrier, which also
+//                frees the page's V tile and P tile;
+//   warps 4 ..   softmax, kSets sets of 4 warps; set s takes the pages with
+//                e % kSets == s and keeps its own running (m, l, o): thread = token
 //                row of S: page max per head, P = exp2 relative to the page max,
 //                scaled by 2^8 and split into two E4M3 terms (value + rounding
 //                remainder) as the B operand of PV; thread = channel: the page's
-//                O folded into the running state.  At the item's end set 1 hands
-//                its state to set 0, which merges the two and writes the
-//                normalised partial (O, LSE).  The LSE merge kernel combines the
-//                splits.
+//                O folded into the running state.  At the item's end sets
+//                1 .. kSets - 1 hand their states to set 0, which merges them and
+//                writes the normalised partial (O, LSE).  The LSE merge kernel
+//                combines the splits;
+//   next 4 kConvSets warps: K conversion, thread = (token, part of the row):
+//                NVFP4 -> FP8 through a 256-entry shared table of scaled E4M3
+//                values and byte permutes, written with tcgen05.st straight into
+//                tensor memory (the A operand);
+//   last 4 kConvSets warps: V conversion, the same into a 128-byte-swizzled
+//                shared-memory tile (3 tiles).
 #include "common.cuh"
 
 namespace msa {
 namespace {
 
 constexpr int kConvSets = 2;   // warps per token row of K (and of V): each converts 4 / kConvSets chunks
-constexpr int kThreads = 32 * (12 + 8 * kConvSets);
+constexpr int kSets = 2;       // softmax sets of 4 warps; set s takes the pages with e % kSets == s
+constexpr int kWarpConv0 = 4 + 4 * kSets;  // first conversion warp
+constexpr int kThreads = 32 * (kWarpConv0 + 8 * kConvSets);
 constexpr int kStages = 6;     // raw K and raw V ring depth
 constexpr int kRecs = 4;       // item records in flight
 constexpr int kK8Slots = 3;    // K8 buffers in tensor memory
 constexpr int kV8Tiles = 3;
 constexpr int kPO = 4;         // P tiles and O buffers
+// a V tile is reused only after the PV of page e - kV8Tiles completes the O
+// barrier of that page; with kV8Tiles <= kPO no later phase of that barrier can
+// complete before the V warps have seen it (that would need page e's V tile)
+static_assert(kV8Tiles <= kPO, "V tile reuse waits on the O barrier of page e - kV8Tiles");
 constexpr int kHalfBytes = kHeadBytes / 2;  // 9,216: codes + scales of K (or V)
 constexpr int kTileBytes = 16384;           // [128 rows][128 B], swizzled
 constexpr int kOffV8 = 0;                                   // kV8Tiles V8 tiles
@@ -58,26 +67,29 @@ constexpr int kOffKRaw = kOffP + kPO * 2048;                // kStages x 9,216
 constexpr int kOffVRaw = kOffKRaw + kStages * kHalfBytes;   // kStages x 9,216
 constexpr int kOffTab = kOffVRaw + kStages * kHalfBytes;    // uint2 [256]
 constexpr int kOffRec = kOffTab + 2048;                     // kRecs x 256 B
-constexpr int kOffMerge = kOffRec + kRecs * 256;            // 2 x (o [4][128], m [4], L [4]) floats
+constexpr int kOffMerge = kOffRec + kRecs * 256;            // [kSets - 1][2] x (o [4][128], m [4], L [4]) floats
 constexpr int kMergeBytes = (4 * 128 + 8) * 4;
-constexpr int kOffBars = kOffMerge + 2 * kMergeBytes;
+constexpr int kMergeBufs = 2 * (kSets - 1);                 // per helper set, per item parity
+constexpr int kOffBars = kOffMerge + kMergeBufs * kMergeBytes;
 // barrier indices
 constexpr int kKrFull = 0, kKrEmpty = kStages, kVrFull = 2 * kStages, kVrEmpty = 3 * kStages;
 constexpr int kK8Full = 4 * kStages, kK8Empty = kK8Full + kK8Slots, kSFull = kK8Empty + kK8Slots,
-              kSEmpty = kSFull + 2, kV8Full = kSEmpty + 2, kV8Empty = kV8Full + kV8Tiles,
-              kPFull = kV8Empty + kV8Tiles, kPEmpty = kPFull + kPO, kOFull = kPEmpty + kPO,
+              kSEmpty = kSFull + kSets, kV8Full = kSEmpty + kSets, kPFull = kV8Full + kV8Tiles,
+              kOFull = kPFull + kPO,
               kOEmpty = kOFull + kPO, kRecFull = kOEmpty + kPO, kRecEmpty = kRecFull + kRecs,
-              kMergeFull = kRecEmpty + kRecs, kMergeEmpty = kMergeFull + 2, kDone = kMergeEmpty + 2,
+              kMergeFull = kRecEmpty + kRecs, kMergeEmpty = kMergeFull + kMergeBufs,
+              kDone = kMergeEmpty + kMergeBufs,
               kNumBars = kDone + 2;  // kDone: QK issuer, kDone + 1: PV issuer
 constexpr int kOffMisc = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;  // tmem, abort, issued K/V
-constexpr int kOffRed = kOffMisc + 16;        // float [2 sets][2][4 warps][4 heads] page maxima
-constexpr int kOffRedL = kOffRed + 256;       // float [2 sets][4 warps][4 heads] row sums
-constexpr int kOffQsl = kOffRedL + 128;       // int [n_seqs + 1] copy of q_start_loc
-constexpr uint32_t kTmS = 32 * kK8Slots;      // TMEM columns: K8 slot i at 32 i, S slots at kTmS,
-constexpr uint32_t kTmO = kTmS + 32;          // kTmS + 16, O buffers at kTmO + 16 i
+constexpr int kOffRed = kOffMisc + 16;        // float [kSets][2][4 warps][4 heads] page maxima
+constexpr int kOffRedL = kOffRed + 128 * kSets;  // float [kSets][4 warps][4 heads] row sums
+constexpr int kOffQsl = kOffRedL + 64 * kSets;   // int [n_seqs + 1] copy of q_start_loc
+constexpr uint32_t kTmS = 32 * kK8Slots;      // TMEM columns: K8 slot i at 32 i, S slot s at kTmS + 16 s,
+constexpr uint32_t kTmO = kTmS + 16 * kSets;  // O buffers at kTmO + 16 i
 constexpr uint32_t kTmemCols = 256;
 static_assert(kTmO + 16 * kPO <= kTmemCols, "tensor memory columns");
-constexpr int kRecEmptyCount = 1 + 8 * kConvSets + 1 + 1 + 8;  // producer, K and V, QK, PV, softmax
+constexpr int kRecEmptyCount = 1 + 8 * kConvSets + 1 + 1 + 4 * kSets;  // producer, K and V, QK, PV, softmax
+static_assert(kPO > kSets, "a set writes P of page e before it folds page e - kSets");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1 KB alignment");
@@ -133,20 +145,17 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
-// Code chunk c (32 channels) of token `row`: 16 code bytes and the two group
-// scales -> 32 FP8 bytes (channels 32c..32c+31) in o[0..7], zeros for a token
-// after pos_j (live false).  Code chunk c sits at position c ^ ((row >> 1) & 3),
-// so chunk c of 8 consecutive rows (64 B apart) lies in 8 different bank groups.
-__device__ __forceinline__ void convert_chunk(const uint8_t* raw, const uint2* tab, int row, int c,
-                                              bool live, uint32_t* o) {
-  const uint4 w = *reinterpret_cast<const uint4*>(raw + row * 64 + 16 * code_chunk_pos(c, row));
-  const uint8_t* sc = raw + kOffKs + row;  // scales [8 groups][128 tokens] after the codes
-  const uint2 t0 = tab[sc[(2 * c) * kPageTokens]];
-  const uint2 t1 = tab[sc[(2 * c + 1) * kPageTokens]];
+// One 32-channel code chunk of a token: 16 code bytes at `codes` and the two
+// group scales at sc[0] and sc[kPageTokens] -> 32 FP8 bytes in o[0..7].
+__device__ __forceinline__ void convert_chunk(const uint8_t* codes, const uint8_t* sc, const uint2* tab,
+                                              uint32_t* o) {
+  const uint4 w = *reinterpret_cast<const uint4*>(codes);
+  const uint2 t0 = tab[sc[0]];
+  const uint2 t1 = tab[sc[kPageTokens]];
   const uint2 a = dequant8(w.x, t0), b = dequant8(w.y, t0);
   const uint2 d = dequant8(w.z, t1), e = dequant8(w.w, t1);
-  o[0] = live ? a.x : 0u; o[1] = live ? a.y : 0u; o[2] = live ? b.x : 0u; o[3] = live ? b.y : 0u;
-  o[4] = live ? d.x : 0u; o[5] = live ? d.y : 0u; o[6] = live ? e.x : 0u; o[7] = live ? e.y : 0u;
+  o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+  o[4] = d.x; o[5] = d.y; o[6] = e.x; o[7] = e.y;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams p) {
@@ -180,19 +189,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       mbar_init(bar(kK8Full + i), 4 * kConvSets);
       mbar_init(bar(kK8Empty + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSets; ++i) {
       mbar_init(bar(kSFull + i), 1);
       mbar_init(bar(kSEmpty + i), 4);
+    }
+    for (int i = 0; i < kMergeBufs; ++i) {
       mbar_init(bar(kMergeFull + i), 4);
       mbar_init(bar(kMergeEmpty + i), 4);
     }
-    for (int i = 0; i < kV8Tiles; ++i) {
-      mbar_init(bar(kV8Full + i), 4 * kConvSets);
-      mbar_init(bar(kV8Empty + i), 1);
-    }
+    for (int i = 0; i < kV8Tiles; ++i) mbar_init(bar(kV8Full + i), 4 * kConvSets);
     for (int i = 0; i < kPO; ++i) {
       mbar_init(bar(kPFull + i), 4);
-      mbar_init(bar(kPEmpty + i), 1);
       mbar_init(bar(kOFull + i), 1);
       mbar_init(bar(kOEmpty + i), 4);
     }
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const int n = rec(slot)->n_pg;
         const uint64_t bdesc = umma_desc_sw128(sbase + kOffQ + slot * 2048);
         for (int i = 0; i < n; ++i, ++e) {
-          const int sl = e & 1, ph = (e >> 1) & 1, ks = e % kK8Slots, kph = (e / kK8Slots) & 1;
+          const int sl = e % kSets, ph = (e / kSets) & 1, ks = e % kK8Slots, kph = (e / kK8Slots) & 1;
           if (!mbar_wait(bar(kK8Full + ks), kph, s_abort) || !mbar_wait(bar(kSEmpty + sl), ph ^ 1, s_abort)) {
             ok = false;
             break;
@@ -357,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const int n = rec(slot)->n_pg;
         mbar_arrive(bar(kRecEmpty + slot));  // nothing else of the record is needed
         for (int i = 0; i < n; ++i, ++e) {
-          const int v = e % kV8Tiles, vph = (e / kV8Tiles) & 1, po = e & 3, pph = (e >> 2) & 1;
+          const int v = e % kV8Tiles, vph = (e / kV8Tiles) & 1, po = e % kPO, pph = (e / kPO) & 1;
           if (!mbar_wait(bar(kV8Full + v), vph, s_abort) || !mbar_wait(bar(kPFull + po), pph, s_abort) ||
               !mbar_wait(bar(kOEmpty + po), pph ^ 1, s_abort)) {
             ok = false;
@@ -372,25 +379,38 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
                 umma_desc_sw128_lbo_sbo(sbase + kOffV8 + v * kTileBytes + kk * 4096, 1024, 1024);
             umma_e4m3(tmem + kTmO + 16 * po, adesc, bdesc + 2 * kk, idesc, kk > 0);
           }
-          umma_commit(bar(kV8Empty + v));
-          umma_commit(bar(kPEmpty + po));
+          // one commit: page e's O is ready, and its V tile and P tile are free
           umma_commit(bar(kOFull + po));
         }
       }
       umma_commit(bar(kDone + 1));
     }
     __syncwarp();
-  } else if (warp >= 12) {
+  } else if (warp >= kWarpConv0) {
     // ---------------- conversion: K (warps 12 ..) or V (the next 4 kConvSets) --------
     // thread = token; the kConvSets warps of a token row take its 16-byte code
     // chunks c = cs * kCh .. cs * kCh + kCh - 1
-    const bool is_k = warp < 12 + 4 * kConvSets;
+    const bool is_k = warp < kWarpConv0 + 4 * kConvSets;
     constexpr int kCh = 4 / kConvSets;
-    const int cs = ((warp - 12) >> 2) % kConvSets;
+    const int cs = ((warp - kWarpConv0) >> 2) % kConvSets;
     // K warps write TMEM lanes 32 (warp % 4) ..; V warps any order
     const int tok = 32 * (warp & 3) + lane;
     const int full0 = is_k ? kKrFull : kVrFull, empty0 = is_k ? kKrEmpty : kVrEmpty;
     const uint32_t raw0 = is_k ? kOffKRaw : kOffVRaw;
+    // Per-thread offsets of this thread's chunks, fixed for the whole kernel:
+    // code chunk c of token tok sits at position c ^ ((tok >> 1) & 3) of its
+    // 64-byte row (8 consecutive tokens hit 8 bank groups), its two group
+    // scales at [2c][tok] and [2c + 1][tok] after the codes; in the V tile
+    // 16-byte chunk j of row tok sits at position j ^ (tok & 7).
+    uint32_t code_off[kCh], sc_off[kCh], v_off[kCh][2];
+#pragma unroll
+    for (int ci = 0; ci < kCh; ++ci) {
+      const int c = cs * kCh + ci;
+      code_off[ci] = tok * 64 + 16 * code_chunk_pos(c, tok);
+      sc_off[ci] = kOffKs + 2 * c * kPageTokens + tok;
+      v_off[ci][0] = tok * 128 + (((2 * c) ^ (tok & 7)) << 4);
+      v_off[ci][1] = tok * 128 + (((2 * c + 1) ^ (tok & 7)) << 4);
+    }
     int e = 0;
     bool ok = true;
     for (int k = 0; ok && k < n_mine; ++k) {
@@ -401,30 +421,43 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       for (int i = 0; i < n; ++i, ++e) {
         const int st = e % kStages;
         // output slot: K8 buffer e % kK8Slots (freed by its previous QK), V8 tile
-        // e % kV8Tiles (freed by its previous PV)
+        // e % kV8Tiles (freed by the PV of page e - kV8Tiles, whose commit
+        // completes the O barrier of that page)
         const int os = is_k ? e % kK8Slots : e % kV8Tiles;
-        const int oph = is_k ? ((e / kK8Slots) & 1) : ((e / kV8Tiles) & 1);
-        if (!warp_wait(bar(full0 + st), (e / kStages) & 1, s_abort) ||
-            !warp_wait(bar((is_k ? kK8Empty : kV8Empty) + os), oph ^ 1, s_abort)) {
+        bool got = warp_wait(bar(full0 + st), (e / kStages) & 1, s_abort);
+        if (got) {
+          if (is_k) {
+            got = warp_wait(bar(kK8Empty + os), ((e / kK8Slots) & 1) ^ 1, s_abort);
+          } else if (e >= kV8Tiles) {
+            const int ev = e - kV8Tiles;
+            got = warp_wait(bar(kOFull + ev % kPO), (ev / kPO) & 1, s_abort);
+          }
+        }
+        if (!got) {
           ok = false;
           break;
         }
-        const bool live = tok < r->valid[i];
+        // tokens after the query position (only in the recent block) become zeros
+        const int valid = r->valid[i];
+        const bool full = valid >= 32 * (warp & 3) + 32;  // warp-uniform
+        const bool live = tok < valid;
         const uint8_t* raw = smem + raw0 + st * kHalfBytes;
-        // K: row tok of A in TMEM, columns 32 os + 8c .. + 7 = channels 32c .. 32c + 31;
-        // V: row tok of the V tile, 16-byte chunk j at position j ^ (tok & 7)
+        // K: row tok of A in TMEM, columns 32 os + 8c .. + 7 = channels 32c .. 32c + 31
         const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * os;
-        uint8_t* dst = smem + kOffV8 + os * kTileBytes + tok * 128;
+        uint8_t* dst = smem + kOffV8 + os * kTileBytes;
 #pragma unroll
         for (int ci = 0; ci < kCh; ++ci) {
-          const int c = cs * kCh + ci;
           uint32_t o[8];
-          convert_chunk(raw, s_tab, tok, c, live, o);
+          convert_chunk(raw + code_off[ci], raw + sc_off[ci], s_tab, o);
+          if (!full) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x) o[x] = live ? o[x] : 0u;
+          }
           if (is_k) {
-            tmem_st8(ta + 8 * c, o);
+            tmem_st8(ta + 8 * (cs * kCh + ci), o);
           } else {
-            *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (tok & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (tok & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint4*>(dst + v_off[ci][0]) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + v_off[ci][1]) = make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
         if (is_k) {
@@ -435,7 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         }
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar((is_k ? kK8Full : kV8Full) + os));
+          if (is_k) mbar_arrive(bar(kK8Full + os));
+          else mbar_arrive(bar(kV8Full + os));
           mbar_arrive(bar(empty0 + st));
         }
       }
@@ -443,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
     }
   }
   else if (warp >= 4) {
-    // ---------------- softmax: set 0 = warps 4-7, set 1 = warps 8-11 ---------------------
-    // set s takes the pages with e % 2 == s; warp w reads TMEM lanes 32 (w % 4) ..:
+    // ---------------- softmax: set s = warps 4 + 4 s .. 7 + 4 s ------------------------
+    // set s takes the pages with e % kSets == s; warp w reads TMEM lanes 32 (w % 4) ..:
     // row = token of S, channel of O
     const int set = (warp - 4) >> 2, quad = warp & 3, row = 32 * quad + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
@@ -469,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       }
       // O of page ef (relative to its page max) -> running state
       auto fold = [&](int ef) -> bool {
-        const int po = ef & 3;
-        if (!warp_wait(bar(kOFull + po), (ef >> 2) & 1, s_abort)) return false;
+        const int po = ef % kPO;
+        if (!warp_wait(bar(kOFull + po), (ef / kPO) & 1, s_abort)) return false;
         tc_fence_after();
         float ov[8];
         tmem_ld8(trow + kTmO + 16 * po, ov);  // columns 0-3: hi terms, 4-7: remainders
@@ -482,8 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         return true;
       };
       int e_prev = -1;
-      for (int e = e0 + ((set - e0) & 1); e < e0 + n; e += 2) {
-        const int ph = (e >> 1) & 1;
+      for (int e = e0 + (set - e0 % kSets + kSets) % kSets; e < e0 + n; e += kSets) {
+        const int ph = (e / kSets) & 1;
         bool good = warp_wait(bar(kSFull + set), ph, s_abort);
         float sv[4] = {0.f, 0.f, 0.f, 0.f};
         if (good) {
@@ -527,8 +561,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         }
         // P rows h (E4M3 of 256 p) and 4+h (E4M3 of the remainder), one byte per
         // token: byte t of row n sits in chunk (t/16) ^ (n & 7)
-        const int po = e & 3;
-        bool step_ok = warp_wait(bar(kPEmpty + po), ((e >> 2) & 1) ^ 1, s_abort);
+        const int po = e % kPO;
+        // P tile po is free once the PV of page e - kPO is done (its O barrier)
+        bool step_ok = warp_wait(bar(kOFull + po), ((e / kPO) & 1) ^ 1, s_abort);
         if (step_ok) {
           uint8_t* pt = smem + kOffP + po * 2048;
 #pragma unroll
@@ -563,10 +598,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       named_barrier_sync(nb, 128);
 #pragma unroll
       for (int h = 0; h < 4; ++h) L[h] = aborted ? 0.f : redl[h] + redl[4 + h] + redl[8 + h] + redl[12 + h];
-      // ---- merge the two sets' states: set 1 hands over, set 0 writes ---------------------
-      const int mb = k & 1, mph = (k >> 1) & 1;
-      float* mo = reinterpret_cast<float*>(smem + kOffMerge + mb * kMergeBytes);  // o [4][128], m [4], L [4]
-      if (set == 1) {
+      // ---- merge the sets' states: sets 1 .. kSets - 1 hand over, set 0 writes ------------
+      const int mph = (k >> 1) & 1;
+      auto merge_buf = [&](int helper) {  // o [4][128], m [4], L [4]
+        return reinterpret_cast<float*>(smem + kOffMerge + (2 * (helper - 1) + (k & 1)) * kMergeBytes);
+      };
+      if (set > 0) {
+        const int mb = 2 * (set - 1) + (k & 1);
+        float* mo = merge_buf(set);
         if (warp_wait(bar(kMergeEmpty + mb), mph ^ 1, s_abort)) {
 #pragma unroll
           for (int h = 0; h < 4; ++h) mo[h * 128 + row] = o_run[h];
@@ -581,22 +620,35 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
           if (lane == 0) mbar_arrive(bar(kMergeFull + mb));
         }
       } else {
-        const bool got = warp_wait(bar(kMergeFull + mb), mph, s_abort);
+        bool got = true;
+#pragma unroll
+        for (int hs = 1; hs < kSets; ++hs)
+          got = warp_wait(bar(kMergeFull + 2 * (hs - 1) + (k & 1)), mph, s_abort) && got;
         const size_t row0 = ((size_t)r->j * p.n_splits + r->split) * kQHeads + r->kvh * kGqa;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const float m1 = got ? mo[512 + h] : -INFINITY, L1 = got ? mo[516 + h] : 0.f;
-          const float o1 = got ? mo[h * 128 + row] : 0.f;
-          const float m = fmaxf(m_run[h], m1);
+          float m = m_run[h];
+#pragma unroll
+          for (int hs = 1; hs < kSets; ++hs) m = fmaxf(m, got ? merge_buf(hs)[512 + h] : -INFINITY);
           const float w0 = (m_run[h] == -INFINITY || L[h] == 0.f) ? 0.f : fast_exp2(m_run[h] - m);
-          const float w1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : fast_exp2(m1 - m);
-          const float Lm = L[h] * w0 + L1 * w1;
+          float Lm = L[h] * w0, om = o_run[h] * w0;
+#pragma unroll
+          for (int hs = 1; hs < kSets; ++hs) {
+            const float* mo = merge_buf(hs);
+            const float m1 = got ? mo[512 + h] : -INFINITY, L1 = got ? mo[516 + h] : 0.f;
+            const float w1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : fast_exp2(m1 - m);
+            Lm += L1 * w1;
+            om += (got ? mo[h * 128 + row] : 0.f) * w1;
+          }
           const bool nonempty = !aborted && got && Lm > 0.f;
-          p.o_part[(row0 + h) * kHeadDim + row] = nonempty ? (o_run[h] * w0 + o1 * w1) / Lm * p.out_scale : 0.f;
+          p.o_part[(row0 + h) * kHeadDim + row] = nonempty ? om / Lm * p.out_scale : 0.f;
           if (row == 0) p.lse_part[row0 + h] = nonempty ? (m + log2f(Lm)) * kLn2 : -INFINITY;
         }
         __syncwarp();
-        if (lane == 0 && got) mbar_arrive(bar(kMergeEmpty + mb));
+        if (lane == 0 && got) {
+#pragma unroll
+          for (int hs = 1; hs < kSets; ++hs) mbar_arrive(bar(kMergeEmpty + 2 * (hs - 1) + (k & 1)));
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kRecEmpty + slot));
