@@ -69,8 +69,9 @@ size_t scan_smem_bytes(int n_seqs) { return 1024 + kOffPrefix + 20 * (size_t)n_s
 
 // Relative cost of scanning one page for a sequence with n_q query tokens: a
 // fixed part per pass of up to 8 tokens (the page's bytes) plus the epilogue's
-// per-token part (measured: a pass with 8 tokens costs about 1.3x one with 1).
-constexpr int kPassCost = 23;
+// per-token part (a least-squares fit of per-CTA scan times on a ragged batch
+// with 1-8 tokens per sequence: a pass with 8 tokens costs about 1.4x one with 1).
+constexpr int kPassCost = 16;
 __device__ __forceinline__ long long page_weight(int n_q) {
   return (long long)((n_q + kNqMax - 1) / kNqMax) * kPassCost + n_q;
 }
