@@ -164,19 +164,36 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
     return;
   }
   // block score = max of the four partial maxima (written by other CTAs: read
-  // through L2)
+  // through L2).  Up to kRegKeys blocks per thread the keys live in registers
+  // (all loads in flight at once, no shared-memory staging); longer rows are
+  // staged in shared memory, or read from L2 each time beyond kTopkStage.
+  constexpr int kRegKeys = 16;
   const float4* row = reinterpret_cast<const float4*>(p.scores + (size_t)j * p.max_pages * 4);
-  const bool staged = r <= kTopkStage;
+  const bool in_regs = r <= kRegKeys * NT;
+  const bool staged = !in_regs && r <= kTopkStage;
+  auto make_key = [](float sc, int blk) -> unsigned long long {
+    return ((unsigned long long)ordered_bits(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
+  };
   auto score = [&](int blk) -> float {
     if (staged) return sm.sc[blk];
     const float4 v = __ldcg(row + blk);
     return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
   };
-  auto key = [&](int blk) -> unsigned long long {
-    return ((unsigned long long)ordered_bits(score(blk)) << 32) |
-           (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
-  };
-  if (staged) {
+  auto key = [&](int blk) -> unsigned long long { return make_key(score(blk), blk); };
+  unsigned long long kr[kRegKeys];  // block tid + u NT; 0 = no block (every real key is > 0)
+  if (in_regs) {
+    float4 v4[kRegKeys];
+#pragma unroll
+    for (int u = 0; u < kRegKeys; ++u) {
+      const int blk = tid + u * NT;
+      v4[u] = blk < r ? __ldcg(row + blk) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kRegKeys; ++u) {
+      const int blk = tid + u * NT;
+      kr[u] = blk < r ? make_key(fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w)), blk) : 0ull;
+    }
+  } else if (staged) {
     // batches of 8 loads in flight per thread, then the stores
     for (int base = tid; base < r; base += 8 * NT) {
       float4 v[8];
@@ -194,30 +211,37 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
   }
   if (tid == 0) sm.misc[0] = 0;
   __syncthreads();
-  // theta: thread t owns blocks t, t + NT, ...  Each warp sorts its 32 thread
-  // maxima (bitonic, by shuffles), so lane i holds the warp's (i+1)-th largest.
-  // For m in {2, 4, 8, 16}: if 16/m warps each have m keys at or above x, then
-  // x <= the 16th largest key; so the (16/m)-th largest of the warps' m-th
-  // largest maxima is a lower bound of the 16th largest key, and theta is the
-  // largest of these four bounds.  Every winner is then a candidate.  (r > 16
-  // here; real keys are distinct and > 0, a missing key counts as 0.)
+  // theta: thread t owns blocks t, t + NT, ...  Each warp sorts the score parts
+  // of its 32 thread maxima (bitonic, by shuffles), so lane i holds the warp's
+  // (i+1)-th largest.  For m in {2, 4, 8, 16}: if 16/m warps each have m keys
+  // at or above x, then x <= the 16th largest key; so the (16/m)-th largest of
+  // the warps' m-th largest maxima (as a key with the block bits clear) is a
+  // lower bound of the 16th largest key, and theta is the largest of these four
+  // bounds.  Every winner is then a candidate.  (r > 16 here; real keys are
+  // distinct and > 0, a missing key counts as 0.)
   constexpr int kNW = NT / 32;
-  unsigned long long v = 0;
-  for (int blk = tid; blk < r; blk += NT) v = umax64(v, key(blk));
+  unsigned long long vmax = 0;
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < kRegKeys; ++u) vmax = umax64(vmax, kr[u]);
+  } else {
+    for (int blk = tid; blk < r; blk += NT) vmax = umax64(vmax, key(blk));
+  }
+  uint32_t v = (uint32_t)(vmax >> 32);
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
     for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, jj);
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, v, jj);
       // descending overall: the lower lane of a pair keeps the larger value in
       // blocks whose bit k is clear, the smaller one where it is set
       const bool lower = (lane & jj) == 0, asc = (lane & k) == 0;
-      v = (lower == asc) ? umax64(v, o) : (v < o ? v : o);
+      v = (lower == asc) ? max(v, o) : min(v, o);
     }
   }
   // tmax[4w + s] = warp w's (2 << s)-th largest maximum; tmax[4 kNW] = theta
   if (lane == 1 || lane == 3 || lane == 7 || lane == 15)
-    sm.tmax[(tid >> 5) * 4 + (31 - __clz(lane + 1)) - 1] = v;
+    sm.tmax[(tid >> 5) * 4 + (31 - __clz(lane + 1)) - 1] = (unsigned long long)v << 32;
   if (tid == 0) sm.tmax[4 * kNW] = 0ull;
   __syncthreads();
   if (tid < 4 * kNW) {
@@ -233,7 +257,12 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
   // candidates: keys >= theta, written without atomics: per-thread counts, a
   // scan over lanes and warps, then each thread writes its own
   int cnt = 0;
-  for (int blk = tid; blk < r; blk += NT) cnt += key(blk) >= theta;
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < kRegKeys; ++u) cnt += kr[u] >= theta;
+  } else {
+    for (int blk = tid; blk < r; blk += NT) cnt += key(blk) >= theta;
+  }
   int incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -250,11 +279,21 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
     nc_all += c;
   }
   if (cnt) {
-    for (int blk = tid; blk < r; blk += NT) {
-      const unsigned long long k = key(blk);
-      if (k >= theta) {
-        if (at < kMaxCand) sm.cand[at] = k;
-        ++at;
+    if (in_regs) {
+#pragma unroll
+      for (int u = 0; u < kRegKeys; ++u) {
+        if (kr[u] >= theta) {
+          if (at < kMaxCand) sm.cand[at] = kr[u];
+          ++at;
+        }
+      }
+    } else {
+      for (int blk = tid; blk < r; blk += NT) {
+        const unsigned long long k = key(blk);
+        if (k >= theta) {
+          if (at < kMaxCand) sm.cand[at] = k;
+          ++at;
+        }
       }
     }
   }
@@ -282,9 +321,15 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
     unsigned long long bound = ~0ull;
     for (int k = 0; k < kTopK; ++k) {
       unsigned long long best = 0;
-      for (int blk = tid; blk < r; blk += NT) {
-        const unsigned long long kk = key(blk);
-        if (kk < bound) best = umax64(best, kk);
+      if (in_regs) {
+#pragma unroll
+        for (int u = 0; u < kRegKeys; ++u)
+          if (kr[u] < bound) best = umax64(best, kr[u]);
+      } else {
+        for (int blk = tid; blk < r; blk += NT) {
+          const unsigned long long kk = key(blk);
+          if (kk < bound) best = umax64(best, kk);
+        }
       }
       sm.tmax[tid] = best;
       __syncthreads();

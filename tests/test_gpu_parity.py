@@ -204,6 +204,27 @@ def test_full_size_config_sampled(cfg):
     assert st.cache.read_status() == 0
 
 
+@pytest.mark.parametrize("ctx", [5121 * 128 + 1, 2_200_000])
+def test_topk_of_long_rows_matches_block_scores(ctx):
+    # Rows of 5,120 blocks (the most the top-k holds in registers) and 5,121
+    # (staged in shared memory), and of more than 16,384 blocks (read from L2
+    # each time): the selection is the exact top-16 of the kernel's own block
+    # scores, ties to the lower block, then the recent block.
+    wl = workloads.custom(f"long_{ctx}", [ctx], [2], seed=91)
+    st = harness.build_state(wl, DEV)
+    bufs, out, S = _decode(wl, st)
+    sel = bufs.sel.cpu().numpy()
+    n_sel = bufs.n_sel.cpu().numpy()
+    for j in range(wl.n_q_total):
+        r = (ctx - wl.n_q_total + j) // 128
+        sc = S[j, :r]
+        order = np.lexsort((np.arange(r), -sc))
+        want = sorted(int(x) for x in order[:16]) + [r]
+        assert [int(x) for x in sel[j, : n_sel[j]]] == want, j
+    assert np.isfinite(out).all()
+    assert st.cache.read_status() == 0
+
+
 def test_host_validation_errors(tiny):
     wl, st, _ = tiny
     q, qi, w = wl.queries(DEV)
