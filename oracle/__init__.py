@@ -20,7 +20,8 @@ Sources (pages on the method):
   * kongchang.com article, section "NVFP4 KV Cache and MoE Weights": NVFP4 is a
     4-bit float with block-wise shared scaling factors.
 The details the pages leave open (scoring formula, tie-break, GQA 16/4, the
-two-level NVFP4 scale, tolerances) are the readings listed in the design doc.
+two-level NVFP4 scale, tolerances) are readings of the pages, each stated in
+the header of the module that implements it.
 
 Parity status per function is stated in each module header.
 """

@@ -7,7 +7,7 @@ same as dense attention (blog, "Sparse attention still scans an index"); FP8
 queries meet K/V dequantised from NVFP4 to FP8 before the matmul (ai4snews
 article, third paragraph; blog, "Capacity savings must pay for conversion").
 
-Readings (listed in the design doc): 16 query heads share 4 KV heads (head h uses
+Readings of the pages (where they are silent): 16 query heads share 4 KV heads (head h uses
 KV head h // 4); logits = (q8 . k8) * softmax_scale / s_enc_K with
 softmax_scale = 1/sqrt(128); out = sum_t p_t v8_t / sum_t p_t / s_enc_V; keys
 at positions after the query token are not visible.

@@ -8,7 +8,7 @@ per query (blog, "Sparse attention still scans an index"); the index holds 128
 FP8 bytes per token and layer (same section).  Selection stays exact when the
 scan is split (blog, "Parallelize index work across context").
 
-Readings (listed in the design doc): the token score is
+Readings of the pages (where they are silent): the token score is
     score(t) = sum_h w_h * max(0, q_h . k_idx(t))
 over the indexer heads h; a block's score is the max over its tokens; token j
 of a sequence sits at pos_j = seq_len - n_q + j and its recent block is

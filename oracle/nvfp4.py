@@ -9,7 +9,7 @@ elements (ai4snews article, second paragraph); queries stay FP8 so the cache
 is dequantised to FP8 before the matmul (same article, third paragraph; blog
 section "Capacity savings must pay for conversion").
 
-Readings (the pages are silent; listed in the design doc):
+Readings (the pages are silent on these):
   * one E4M3 scale per 16 consecutive channels of one token and head, plus an
     fp32 per-tensor encode scale ``s_enc = fp32(448 / amax)`` over the whole
     K (resp. V) tensor, so that a dequantised element (<= 6 x 72) never
