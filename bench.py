@@ -246,12 +246,18 @@ def run_gpu(args, rank, world, local_rank):
     e2e = float(np.mean(e2e_ms))
 
     if world > 1:
-        t = torch.tensor([ms, t_idx, e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, t_idx, e2e = (float(x) for x in t.cpu())
+        ms, t_idx, e2e = max_over_ranks([ms, t_idx, e2e], dev)
     return dict(wl=wl, T=T, ms=ms, t_idx=t_idx, e2e=e2e, h2d=h2d, d2h=d2h, n_splits=n_splits,
                 idx_bytes=idx_bytes, kv_bytes=kv_bytes, alg_bytes=alg_bytes, clocks=clk,
                 launches=(3 if n_splits > 1 else 2) * args.steps)
+
+
+def max_over_ranks(values, device):
+    """Element-wise max of a list of floats over all ranks of the process group:
+    the slowest replica sets each time."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
 
 
 def oracle_sample(wl, device, budget_s):
