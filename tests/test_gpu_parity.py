@@ -225,6 +225,23 @@ def test_topk_of_long_rows_matches_block_scores(ctx):
     assert st.cache.read_status() == 0
 
 
+def test_most_sequences_per_call():
+    # 4,096 sequences, the most one call takes (the sequence metadata in shared
+    # memory at its largest): short contexts where every block is selected and
+    # longer ones where 16 of up to 20 blocks compete
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(129, 2600, 4096)]
+    wl = workloads.custom("many_seqs", lens, [1] * 4096, seed=55)
+    st = harness.build_state(wl, DEV)
+    side = OracleSide(wl, DEV)
+    bufs, out, S = _decode(wl, st)
+    T = wl.n_q_total
+    tokens = sorted(set([0, 1, T // 2, T - 1] + [int(x) for x in rng.integers(0, T, 3)]))
+    _check_tokens(wl, side, bufs, out, S, tokens)
+    assert np.isfinite(out).all()
+    assert st.cache.read_status() == 0
+
+
 def test_host_validation_errors(tiny):
     wl, st, _ = tiny
     q, qi, w = wl.queries(DEV)
