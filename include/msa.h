@@ -209,6 +209,10 @@ int msa_indexer_topk_noalloc(const msa_cache* cache, const uint8_t* q_idx, const
  * logits = (q . k8) * softmax_scale / s_enc_k; the value contraction is
  * divided by s_enc_v.  Keys after pos_j are masked.  Limits: n_seqs <= 4096,
  * n_q_total <= 65535 (else MSA_ERR_UNSUPPORTED_SHAPE).
+ * Launched as a programmatic dependent of the previous kernel in the stream
+ * (msa_indexer_topk lets it start early): it waits for that kernel before it
+ * reads sel and n_sel, but copies q_start_loc before the wait, so the kernel
+ * just before it must not write q_start_loc.
  */
 int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q_heads,
                            float softmax_scale, const int32_t* sel, const int32_t* n_sel,
