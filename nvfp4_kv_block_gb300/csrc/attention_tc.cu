@@ -34,11 +34,11 @@
 //                1 .. kSets - 1 hand their states to set 0, which merges them and
 //                writes the normalised partial (O, LSE).  The LSE merge kernel
 //                combines the splits;
-//   next 4 kConvSets warps: K conversion, thread = (token, part of the row):
+//   next 4 x kConvSets warps: K conversion, thread = (token, part of the row):
 //                NVFP4 -> FP8 through a 256-entry shared table of scaled E4M3
 //                values and byte permutes, written with tcgen05.st straight into
 //                tensor memory (the A operand);
-//   last 4 kConvSets warps: V conversion, the same into a 128-byte-swizzled
+//   last 4 x kConvSets warps: V conversion, the same into a 128-byte-swizzled
 //                shared-memory tile (3 tiles).
 #include "common.cuh"
 
