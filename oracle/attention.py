@@ -53,19 +53,6 @@ def attend(q8, k8, v8, softmax_scale, s_enc_k, s_enc_v):
     return out, lse
 
 
-def attend_values(q, k, v, scale):
-    """Same contraction on already-decoded float64 values (used for the
-    information-only exact-NVFP4 comparison)."""
-    hq = q.shape[0]
-    out = np.zeros((hq, q.shape[1]))
-    for h in range(hq):
-        g = h // GQA
-        logits = (k[:, g, :] @ q[h]) * scale
-        p = np.exp(logits - logits.max())
-        out[h] = (p @ v[:, g, :]) / p.sum()
-    return out
-
-
 def visible_positions(selection, pos, page_tokens=128):
     """Token positions of the selected blocks that are at or before pos."""
     idx = []

@@ -35,8 +35,7 @@ def decode_e2m1(code):
     return sign * mag
 
 
-def decode_e4m3(byte):
-    """Value of E4M3FN bytes (array of ints 0..255) as float64 (NaN for 0x7F/0xFF)."""
+def _decode_e4m3_fields(byte):
     b = np.asarray(byte, dtype=np.int64)
     sign = np.where((b >> 7) & 1, -1.0, 1.0)
     e = (b >> 3) & 15
@@ -46,6 +45,19 @@ def decode_e4m3(byte):
     mag = np.where(e == 0, sub, nrm)
     mag = np.where((e == 15) & (m == 7), np.nan, mag)
     return sign * mag
+
+
+# Values of all 256 bytes, from the bit fields above; large uint8 arrays are
+# decoded by looking their bytes up here (same values, one gather).
+_E4M3_ALL = _decode_e4m3_fields(np.arange(256))
+
+
+def decode_e4m3(byte):
+    """Value of E4M3FN bytes (array of ints 0..255) as float64 (NaN for 0x7F/0xFF)."""
+    b = np.asarray(byte)
+    if b.dtype == np.uint8:
+        return _E4M3_ALL[b]
+    return _decode_e4m3_fields(b)
 
 
 # The 127 non-negative finite E4M3 values, indexed by their code 0x00..0x7E.

@@ -21,9 +21,12 @@ is a multiple of 2^-18 below 2^18, so a 128-term dot product is exact in
 float64.  The weighted sum over heads is float64.
 
 Parity: pinned (tests/test_oracle_indexer.py) by exact rational dot products,
-a brute-force top-k over all subsets of tiny inputs, a full-sort cross-check,
-the "r <= 16 selects everything" case, the split-scan merge and the worked
-example of tests/golden/indexer_tiny.txt.
+a closed-form one-hot example, a brute-force top-k over all subsets of tiny
+inputs, a full-sort cross-check, the "r <= 16 selects everything" case, the
+split-scan merge, and the hand-computed case of tests/golden/indexer_tiny.txt
+(19 blocks of sparse one-hot keys: block maxima at the first and the last
+token of a block, ReLU of negative dots, a tie at the cut-off, and a recent
+block whose score exceeds every other but does not compete).
 """
 
 import numpy as np
@@ -45,10 +48,18 @@ def token_scores(q_idx, w, keys):
     return np.maximum(dots, 0.0) @ np.asarray(w, dtype=np.float64)
 
 
-def block_scores(q_idx, w, keys, n_blocks):
-    """Per-block max of token scores for blocks 0..n_blocks-1 (full blocks)."""
-    s = token_scores(q_idx, w, keys[: n_blocks * PAGE_TOKENS])
-    return s.reshape(n_blocks, PAGE_TOKENS).max(axis=1) if n_blocks else np.zeros(0)
+def block_scores(q_idx, w, keys, n_blocks, chunk_blocks=4096):
+    """Per-block max of token scores for blocks 0..n_blocks-1 (full blocks).
+
+    Token scores are independent of one another, so the blocks are scored
+    ``chunk_blocks`` at a time only to bound the memory of the decoded keys.
+    """
+    out = np.zeros(n_blocks)
+    for b0 in range(0, n_blocks, chunk_blocks):
+        b1 = min(n_blocks, b0 + chunk_blocks)
+        s = token_scores(q_idx, w, keys[b0 * PAGE_TOKENS: b1 * PAGE_TOKENS])
+        out[b0:b1] = s.reshape(b1 - b0, PAGE_TOKENS).max(axis=1)
+    return out
 
 
 def select(scores, recent, topk=16):

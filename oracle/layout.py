@@ -5,7 +5,7 @@ Test infrastructure only (see ``oracle/__init__``).
 The pages fix the sizes: 128-token blocks (blog, "Sparse attention still scans
 an index"), 128 index bytes per token and layer (same section), and NVFP4 K+V
 at 576 bytes per token and layer for 4 KV heads of dimension 128 (ai4snews
-article, second paragraph: 34,560 bytes/token over the model's layers).  The
+article, first paragraph: 34,560 bytes/token over the model's layers).  The
 placement of bytes inside a page is this library's own format, restated here
 independently of the CUDA code from its written specification:
 

@@ -5,7 +5,7 @@ Test infrastructure only (see ``oracle/__init__``).
 What the pages fix: the K/V cache is NVFP4, a 4-bit float with block-wise
 shared scales (kongchang.com article, "NVFP4 KV Cache and MoE Weights");
 34,560 vs 61,440 bytes/token, i.e. 4 bits plus one byte of scale per 16
-elements (ai4snews article, second paragraph); queries stay FP8 so the cache
+elements (ai4snews article, first paragraph); queries stay FP8 so the cache
 is dequantised to FP8 before the matmul (same article, third paragraph; blog
 section "Capacity savings must pay for conversion").
 

@@ -117,3 +117,74 @@ def test_sequence_positions_and_recent_blocks():
         ts = indexer.token_scores(q[j], w[j], keys[: r * 128]).reshape(r, 128)
         assert np.array_equal(scs[j], ts.max(axis=1))
     assert sels[0][-1] == 19 and sels[-1][-1] == 20
+
+
+def _golden_indexer_tiny():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "indexer_tiny.txt")
+    keys, scores, sel = [], {}, None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            if parts[0] == "key":
+                keys.append((int(parts[1]), int(parts[2]), float(parts[3]), float(parts[4])))
+            elif parts[0] == "score":
+                scores[int(parts[1])] = float(parts[2])
+            elif parts[0] == "sel":
+                sel = [int(x) for x in parts[1:]]
+    return keys, scores, sel
+
+
+def golden_indexer_inputs():
+    """(q_idx uint8 [8,128], w [8], fp32 keys [2309,128], seq_len) of the hand case."""
+    keys, _, _ = _golden_indexer_tiny()
+    seq_len = 2309
+    k = np.zeros((seq_len, 128), dtype=np.float32)
+    for blk, off, k0, k1 in keys:
+        k[blk * 128 + off, 0] = k0
+        k[blk * 128 + off, 1] = k1
+    q = np.zeros((8, 128))
+    q[0, 0] = 1.0
+    q[1, 1] = 2.0
+    w = np.array([1.0, 0.5] + [0.3] * 6, dtype=np.float32)
+    return formats.encode_e4m3(q), w, k, seq_len
+
+
+def test_hand_computed_block_scores_and_selection():
+    _, want_scores, want_sel = _golden_indexer_tiny()
+    q, w, k, seq_len = golden_indexer_inputs()
+    keys = formats.encode_e4m3(k.astype(np.float64))
+    # every listed key value is exact in E4M3
+    assert np.array_equal(formats.decode_e4m3(keys), k.astype(np.float64))
+    r = (seq_len - 1) // 128
+    assert r == 18
+    s = indexer.block_scores(q, w, keys, r)
+    assert [float(x) for x in s] == [want_scores[b] for b in range(r)]
+    assert indexer.select(s, r) == want_sel
+    sels, scs = indexer.sequence_topk(q[None], w[None], keys, seq_len)
+    assert sels[0] == want_sel and np.array_equal(scs[0], s)
+    # the recent block outscores every competing block, yet is not a competitor
+    assert indexer.token_scores(q, w, keys[18 * 128 + 2: 18 * 128 + 3])[0] == 896.0
+
+
+def test_block_scores_are_independent_of_the_chunking():
+    rng = np.random.default_rng(21)
+    keys = _fp8(rng, (40 * 128, 128))
+    q = _fp8(rng, (8, 128))
+    w = rng.uniform(0, 1, 8).astype(np.float32)
+    a = indexer.block_scores(q, w, keys, 40)
+    for chunk in (1, 3, 7, 40, 4096):
+        assert np.array_equal(indexer.block_scores(q, w, keys, 40, chunk_blocks=chunk), a)
+    # and equal to the per-block max written out token by token
+    ts = indexer.token_scores(q, w, keys)
+    assert all(a[b] == max(ts[b * 128:(b + 1) * 128]) for b in range(40))
+
+
+def test_decode_table_equals_the_bit_field_definition():
+    b = np.arange(256, dtype=np.uint8)
+    fast = formats.decode_e4m3(b)
+    slow = formats.decode_e4m3(b.astype(np.int64))
+    assert np.array_equal(np.isnan(fast), np.isnan(slow))
+    assert np.array_equal(fast[~np.isnan(fast)], slow[~np.isnan(slow)])
