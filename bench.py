@@ -6,6 +6,11 @@ is one split: its output is final) over one batch of resident query tokens.  Pri
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl gb300|reference]
 
+The default workload is the largest single-GPU one (--config 4: 64 ragged
+sequences of 30,720-215,040 tokens with 1-8 query tokens each, pages at random
+pool positions); --config 0..3 run the tiny, batched, speculative-verify and
+512K long-context workloads.
+
 --impl reference times the CPU oracle (the plain float64 restatement of the
 method; there is no other reference implementation) on a bounded sample of
 the same workload on this host's cores.
@@ -245,11 +250,50 @@ def run_gpu(args, rank, world, local_rank):
             e2e_ms.append(e0.elapsed_time(e1))
     e2e = float(np.mean(e2e_ms))
 
+    ins = time_insert(args, flush, stream, dev) if args.insert_tokens > 0 else None
+
     if world > 1:
         ms, t_idx, e2e = max_over_ranks([ms, t_idx, e2e], dev)
     return dict(wl=wl, T=T, ms=ms, t_idx=t_idx, e2e=e2e, h2d=h2d, d2h=d2h, n_splits=n_splits,
                 idx_bytes=idx_bytes, kv_bytes=kv_bytes, alg_bytes=alg_bytes, clocks=clk,
-                launches=(3 if n_splits > 1 else 2) * args.steps)
+                launches=(3 if n_splits > 1 else 2) * args.steps, insert=ins)
+
+
+# Algorithmic bytes of inserting one token: fp32 K and V (2 x 4 x 128 x 4), the
+# fp32 index key (128 x 4) and its int64 slot read; NVFP4 K and V (576 B: codes
+# and scales) and the FP8 index key (128 B) written.
+INSERT_READ_BYTES = 2 * 4 * 128 * 4 + 128 * 4 + 8
+INSERT_WRITE_BYTES = 576 + 128
+
+
+def time_insert(args, flush, stream, dev):
+    """Quantise-insert of a batch of new tokens into random slots of a scratch
+    pool (off the decode step; reported as its own sub-measurement)."""
+    n = args.insert_tokens
+    pages = (n + 127) // 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(12345)
+    k = torch.randn((n, 4, 128), generator=g, device=dev)
+    v = torch.randn((n, 4, 128), generator=g, device=dev)
+    ik = torch.randn((n, 128), generator=g, device=dev)
+    slots = torch.randperm(pages * 128, generator=g, device=dev)[:n].to(torch.int64)
+    cache = ops.KVCache(pages, 448.0 / 6.0, 448.0 / 6.0, dev)
+    for _ in range(args.warmup):
+        ops.quantize_kv_insert(cache, k, v, ik, slots)
+    ts = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ops.quantize_kv_insert(cache, k, v, ik, slots)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = float(np.mean(ts))
+    byts = n * (INSERT_READ_BYTES + INSERT_WRITE_BYTES)
+    return {"kernel": "quantize_insert_kernel (msa_quantize_kv_insert)", "tokens": n,
+            "slots": "random permutation of the pool", "ms_per_launch": ms,
+            "algorithmic_bytes_per_launch": byts, "achieved_gbs": byts / (ms * 1e-3) / 1e9}
 
 
 def max_over_ranks(values, device):
@@ -319,7 +363,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1)
+    # default: the largest single-GPU workload (64 ragged sequences, 30K-215K
+    # context, 1-8 query tokens each, 297 in all)
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--insert-tokens", type=int, default=262144,
+                    help="tokens of the timed quantise-insert sub-measurement (0: skip)")
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -383,6 +431,11 @@ def main():
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e"]},
         "gpu_launches": r["launches"], "n_splits": r["n_splits"], "clocks": r["clocks"],
     }
+    if r["insert"] is not None:
+        ins = dict(r["insert"])
+        ins["frac"] = ins["achieved_gbs"] / peak
+        ins["peak_kind"] = peak_kind
+        line["quantize_insert"] = ins
     if not args.no_cpu_baseline:
         qps_cpu, cores, sample = oracle_sample(r["wl"], "cuda", args.cpu_budget)
         line["cpu_baseline"] = {"value": qps_cpu, "unit": "queries/s", "cores": cores, "kind": "oracle",

@@ -5,7 +5,7 @@
  * What the path computes (sources: "vLLM Delivers Day-0 Support for
  * MiniMax-M3.1-Flash", yuxiaoba.github.io, sections "Sparse attention still
  * scans an index" and "Capacity savings must pay for conversion"; ai4snews
- * article on MiniMax-M3.1-Flash in vLLM, second and third paragraphs;
+ * article on MiniMax-M3.1-Flash in vLLM, first and third paragraphs;
  * kongchang.com article, "NVFP4 KV Cache and MoE Weights"):
  *   - the KV cache lives in 128-token blocks (pages), K and V stored as NVFP4:
  *     E2M1 values with one E4M3 scale per 16 channels and an fp32 per-tensor
@@ -84,6 +84,10 @@ typedef struct CUstream_st* msa_stream_t; /* same type as cudaStream_t */
 #define MSA_STATUS_BAD_SEQ 0x4        /* n_q < 0, n_q > seq_len or seq_len > max_pages*128 */
 #define MSA_STATUS_BAD_SELECTION 0x8  /* a selected block id outside 0..r_j */
 #define MSA_STATUS_TIMEOUT 0x10       /* a bounded on-chip wait gave up (results invalid) */
+/* Every on-chip wait is bounded (2 s by default): a wait that runs out sets
+ * MSA_STATUS_TIMEOUT, the kernel abandons its work, waits (bounded) for its own
+ * copies and tensor-core operations in flight, releases tensor memory and
+ * returns.  The context stays usable. */
 
 /* The KV cache and its metadata.  Caller-owned; the library only reads it. */
 typedef struct msa_cache {
@@ -101,7 +105,7 @@ typedef struct msa_cache {
 
 /*
  * Quantise new tokens to NVFP4 / FP8 and write them into their cache slots.
- * (NVFP4 KV cache: ai4snews article, second and third paragraphs; index keys of
+ * (NVFP4 KV cache: ai4snews article, first and third paragraphs; index keys of
  * 128 FP8 bytes per token: blog, "Sparse attention still scans an index".)
  *
  *   k, v         fp32 [n_tokens][4][128], row-major, contiguous.
@@ -136,9 +140,10 @@ int msa_quantize_kv_insert(const msa_cache* cache, const float* k, const float* 
  *               the lower id) in ascending order, then r_j; padded with -1.
  *   n_sel       int32 [n_q_total] out: min(topk, r_j) + 1.
  *   ws, ws_bytes scratch of at least msa_indexer_workspace_bytes(...) bytes,
- *               16-byte aligned, ZEROED before its first use (every call leaves
- *               its first 256 bytes -- grid-barrier words -- as it found them
- *               up to a generation count, so later calls need no clearing).  From
+ *               16-byte aligned, ZEROED before its first use.  Its first 256
+ *               bytes hold grid-barrier words; every call, also one whose
+ *               barrier timed out, leaves them at rest (a generation count
+ *               apart), so later calls need no clearing.  From
  *               byte 256, after the stream reaches the end of this call, it holds
  *               for every query token j and block i < r_j four fp32 partial
  *               maxima P[j][i][0..3] (row stride 4 * max_pages floats): the maxima
@@ -181,7 +186,8 @@ size_t msa_indexer_workspace_bytes(int32_t n_q_total, int32_t max_pages);
  * device looks up the array's device address (with that device current);
  * make that first call before any stream capture.  No cudaMalloc, cudaFree
  * or allocating routine is called.  (The array starts zeroed when the library
- * is loaded; its grid-barrier words return to rest after every call.)
+ * is loaded; its grid-barrier words return to rest after every call, also
+ * after one that timed out.)
  */
 int msa_indexer_topk_noalloc(const msa_cache* cache, const uint8_t* q_idx, const float* w,
                              int32_t n_idx_heads, const int32_t* block_table, int32_t max_pages,
@@ -222,14 +228,21 @@ int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q
                            float* o_part, float* lse_part, msa_stream_t stream);
 
 /*
- * Log-sum-exp merge of the split partials:
+ * Log-sum-exp merge of the split partials (blog, "Sparse attention still scans
+ * an index": attention over the selected blocks is exact; a split computes it
+ * over part of them, and the parts combine by their softmax normalisers):
  *   out[j][h] = sum_s exp(lse[j][s][h] - L) * o_part[j][s][h],
  *   L = log sum_s exp(lse[j][s][h]).
- *   out fp32 [n_q_total][n_q_heads][128].  A row whose splits are all empty
- *   is written as zeros.
+ *   out  fp32 [n_q_total][n_q_heads][128].  A row whose splits are all empty
+ *        is written as zeros.
+ *   lse  fp32 [n_q_total][n_q_heads] out, or NULL: the merged L (-inf for a
+ *        row whose splits are all empty), so that merged results can be merged
+ *        again.
+ * Limits: n_q_heads <= 1024, n_q_total <= 65535 (else MSA_ERR_UNSUPPORTED_SHAPE).
  */
 int msa_merge_splits(const float* o_part, const float* lse_part, int32_t n_q_total,
-                     int32_t n_q_heads, int32_t n_splits, float* out, msa_stream_t stream);
+                     int32_t n_q_heads, int32_t n_splits, float* out, float* lse,
+                     msa_stream_t stream);
 
 /*
  * Helpers for the per-tensor scale.  msa_absmax folds max|x[i]| over n fp32
@@ -248,6 +261,22 @@ float msa_encode_scale(float amax);
  */
 int msa_debug_fp8_page(const msa_cache* cache, int64_t page, uint8_t* k8, uint8_t* v8,
                        msa_stream_t stream);
+
+/*
+ * Test hook for the failure paths (the pages have no counterpart).  Sets, for
+ * every later launch of the library in this process, the time limit of one
+ * bounded on-chip wait (wait_limit_ns; 0 restores the default of 2 s) and the
+ * fault-injection flags (0 = none):
+ *   MSA_INJECT_BARRIER_TIMEOUT  the indexer's grid barrier waits for one CTA
+ *                               more than the launch has, so every CTA's wait
+ *                               runs out after wait_limit_ns: the call sets
+ *                               MSA_STATUS_TIMEOUT, leaves sel/n_sel unwritten
+ *                               and its workspace barrier word at rest.
+ * Launches already captured into a CUDA graph keep the settings they were
+ * captured with.  Unknown flags return MSA_ERR_INVALID_ARG.
+ */
+#define MSA_INJECT_BARRIER_TIMEOUT 0x1
+int msa_debug_set_fault_injection(int32_t flags, uint64_t wait_limit_ns);
 
 /* Copies the device status word to *host_out (synchronous on the stream). */
 int msa_read_status(const msa_cache* cache, int32_t* host_out, msa_stream_t stream);

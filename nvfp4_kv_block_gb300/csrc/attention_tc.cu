@@ -126,6 +126,7 @@ struct AttnParams {
   float* o_part;     // [T][S][16][128]
   float* lse_part;   // [T][S][16]
   int* status;
+  unsigned long long wait_ns;  // limit of one bounded wait
 };
 
 // OR of a predicate over the threads of a named barrier (all of them wait).
@@ -141,8 +142,8 @@ __device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred
 }
 
 // Every lane of the warp waits; the result is the same for all of them.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
 }
 
 // One 32-channel code chunk of a token: 16 code bytes at `codes` and the two
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   auto bar = [&](int i) { return sbase + kOffBars + 8 * i; };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  const WaitCtl wc{s_abort, p.wait_ns};
   int* s_issued_k = reinterpret_cast<int*>(smem + kOffMisc + 8);
   int* s_issued_v = reinterpret_cast<int*>(smem + kOffMisc + 12);
   uint2* s_tab = reinterpret_cast<uint2*>(smem + kOffTab);
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
     // ---------------- scheduler: item records ------------------------------------------
     for (int k = 0; k < n_mine; ++k) {
       const int slot = k % kRecs;
-      if (!warp_wait(bar(kRecEmpty + slot), ((k / kRecs) & 1) ^ 1, s_abort)) break;
+      if (!warp_wait(bar(kRecEmpty + slot), ((k / kRecs) & 1) ^ 1, wc)) break;
       const int item = blockIdx.x + k * G;
       const int split = item % p.n_splits, kvh = (item / p.n_splits) % kKvHeads;
       const int j = item / (p.n_splits * kKvHeads);
@@ -299,18 +301,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       bool ok = true;
       for (int k = 0; ok && k < n_mine; ++k) {
         const int slot = k % kRecs;
-        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort)) break;
+        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc)) break;
         const ItemRec* r = rec(slot);
         const int n = r->n_pg;
         const uint8_t* head = p.kv_pool + (size_t)r->kvh * kHeadBytes;
         for (int i = 0; i < n; ++i, ++e) {
           const int st = e % kStages, ph = (e / kStages) & 1;
           const uint8_t* src = head + (size_t)r->phys[i] * kKvPageBytes;
-          if (!mbar_wait(bar(kKrEmpty + st), ph ^ 1, s_abort)) { ok = false; break; }
+          if (!mbar_wait(bar(kKrEmpty + st), ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(kKrFull + st), kHalfBytes);
           bulk_g2s(sbase + kOffKRaw + st * kHalfBytes, src, kHalfBytes, bar(kKrFull + st));
           *s_issued_k = e + 1;
-          if (!mbar_wait(bar(kVrEmpty + st), ph ^ 1, s_abort)) { ok = false; break; }
+          if (!mbar_wait(bar(kVrEmpty + st), ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(kVrFull + st), kHalfBytes);
           bulk_g2s(sbase + kOffVRaw + st * kHalfBytes, src + kHalfBytes, kHalfBytes, bar(kVrFull + st));
           *s_issued_v = e + 1;
@@ -328,12 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       bool ok = true;
       for (int k = 0; ok && k < n_mine; ++k) {
         const int slot = k % kRecs;
-        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort)) break;
+        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc)) break;
         const int n = rec(slot)->n_pg;
         const uint64_t bdesc = umma_desc_sw128(sbase + kOffQ + slot * 2048);
         for (int i = 0; i < n; ++i, ++e) {
           const int sl = e % kSets, ph = (e / kSets) & 1, ks = e % kK8Slots, kph = (e / kK8Slots) & 1;
-          if (!mbar_wait(bar(kK8Full + ks), kph, s_abort) || !mbar_wait(bar(kSEmpty + sl), ph ^ 1, s_abort)) {
+          if (!mbar_wait(bar(kK8Full + ks), kph, wc) || !mbar_wait(bar(kSEmpty + sl), ph ^ 1, wc)) {
             ok = false;
             break;
           }
@@ -360,13 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       bool ok = true;
       for (int k = 0; ok && k < n_mine; ++k) {
         const int slot = k % kRecs;
-        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort)) break;
+        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc)) break;
         const int n = rec(slot)->n_pg;
         mbar_arrive(bar(kRecEmpty + slot));  // nothing else of the record is needed
         for (int i = 0; i < n; ++i, ++e) {
           const int v = e % kV8Tiles, vph = (e / kV8Tiles) & 1, po = e % kPO, pph = (e / kPO) & 1;
-          if (!mbar_wait(bar(kV8Full + v), vph, s_abort) || !mbar_wait(bar(kPFull + po), pph, s_abort) ||
-              !mbar_wait(bar(kOEmpty + po), pph ^ 1, s_abort)) {
+          if (!mbar_wait(bar(kV8Full + v), vph, wc) || !mbar_wait(bar(kPFull + po), pph, wc) ||
+              !mbar_wait(bar(kOEmpty + po), pph ^ 1, wc)) {
             ok = false;
             break;
           }
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
     bool ok = true;
     for (int k = 0; ok && k < n_mine; ++k) {
       const int slot = k % kRecs;
-      if (!warp_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort)) break;
+      if (!warp_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc)) break;
       const ItemRec* r = rec(slot);
       const int n = r->n_pg;
       for (int i = 0; i < n; ++i, ++e) {
@@ -424,13 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         // e % kV8Tiles (freed by the PV of page e - kV8Tiles, whose commit
         // completes the O barrier of that page)
         const int os = is_k ? e % kK8Slots : e % kV8Tiles;
-        bool got = warp_wait(bar(full0 + st), (e / kStages) & 1, s_abort);
+        bool got = warp_wait(bar(full0 + st), (e / kStages) & 1, wc);
         if (got) {
           if (is_k) {
-            got = warp_wait(bar(kK8Empty + os), ((e / kK8Slots) & 1) ^ 1, s_abort);
+            got = warp_wait(bar(kK8Empty + os), ((e / kK8Slots) & 1) ^ 1, wc);
           } else if (e >= kV8Tiles) {
             const int ev = e - kV8Tiles;
-            got = warp_wait(bar(kOFull + ev % kPO), (ev / kPO) & 1, s_abort);
+            got = warp_wait(bar(kOFull + ev % kPO), (ev / kPO) & 1, wc);
           }
         }
         if (!got) {
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
     bool ok = true;
     for (int k = 0; ok && k < n_mine; ++k) {
       const int slot = k % kRecs;
-      if (named_barrier_or(nb, 128, !warp_wait(bar(kRecFull + slot), (k / kRecs) & 1, s_abort))) break;
+      if (named_barrier_or(nb, 128, !warp_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc))) break;
       const ItemRec* r = rec(slot);
       const int n = r->n_pg;
       float m_run[4], l_run[4], o_run[4], a_prev[4], b_prev[4];
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       // O of page ef (relative to its page max) -> running state
       auto fold = [&](int ef) -> bool {
         const int po = ef % kPO;
-        if (!warp_wait(bar(kOFull + po), (ef / kPO) & 1, s_abort)) return false;
+        if (!warp_wait(bar(kOFull + po), (ef / kPO) & 1, wc)) return false;
         tc_fence_after();
         float ov[8];
         tmem_ld8(trow + kTmO + 16 * po, ov);  // columns 0-3: hi terms, 4-7: remainders
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       int e_prev = -1;
       for (int e = e0 + (set - e0 % kSets + kSets) % kSets; e < e0 + n; e += kSets) {
         const int ph = (e / kSets) & 1;
-        bool good = warp_wait(bar(kSFull + set), ph, s_abort);
+        bool good = warp_wait(bar(kSFull + set), ph, wc);
         float sv[4] = {0.f, 0.f, 0.f, 0.f};
         if (good) {
           tc_fence_after();
@@ -563,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         // token: byte t of row n sits in chunk (t/16) ^ (n & 7)
         const int po = e % kPO;
         // P tile po is free once the PV of page e - kPO is done (its O barrier)
-        bool step_ok = warp_wait(bar(kOFull + po), ((e / kPO) & 1) ^ 1, s_abort);
+        bool step_ok = warp_wait(bar(kOFull + po), ((e / kPO) & 1) ^ 1, wc);
         if (step_ok) {
           uint8_t* pt = smem + kOffP + po * 2048;
 #pragma unroll
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       if (set > 0) {
         const int mb = 2 * (set - 1) + (k & 1);
         float* mo = merge_buf(set);
-        if (warp_wait(bar(kMergeEmpty + mb), mph ^ 1, s_abort)) {
+        if (warp_wait(bar(kMergeEmpty + mb), mph ^ 1, wc)) {
 #pragma unroll
           for (int h = 0; h < 4; ++h) mo[h * 128 + row] = o_run[h];
           if (row == 0) {
@@ -623,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         bool got = true;
 #pragma unroll
         for (int hs = 1; hs < kSets; ++hs)
-          got = warp_wait(bar(kMergeFull + 2 * (hs - 1) + (k & 1)), mph, s_abort) && got;
+          got = warp_wait(bar(kMergeFull + 2 * (hs - 1) + (k & 1)), mph, wc) && got;
         const size_t row0 = ((size_t)r->j * p.n_splits + r->split) * kQHeads + r->kvh * kGqa;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -662,9 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   __syncthreads();
   if (tid == 0) {
     // every tcgen05.mma is done (both issuers committed after their last one)
-    volatile int ignore = 0;
-    mbar_wait(bar(kDone), 0, &ignore);
-    mbar_wait(bar(kDone + 1), 0, &ignore);
+    mbar_wait_drain(bar(kDone), 0, p.wait_ns);
+    mbar_wait_drain(bar(kDone + 1), 0, p.wait_ns);
     if (*s_abort) {
       set_status(p.status, MSA_STATUS_TIMEOUT);
       // bounded drain of the copies that may still be landing: the last kStages
@@ -672,9 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       // refilled)
       const int nk = *s_issued_k, nv = *s_issued_v;
       for (int e = max(0, nk - kStages); e < nk; ++e)
-        mbar_wait(bar(kKrFull + e % kStages), (e / kStages) & 1, &ignore);
+        mbar_wait_drain(bar(kKrFull + e % kStages), (e / kStages) & 1, p.wait_ns);
       for (int e = max(0, nv - kStages); e < nv; ++e)
-        mbar_wait(bar(kVrFull + e % kStages), (e / kStages) & 1, &ignore);
+        mbar_wait_drain(bar(kVrFull + e % kStages), (e / kStages) & 1, p.wait_ns);
     }
   }
   __syncthreads();
@@ -692,26 +693,19 @@ cudaError_t launch_sparse_attn_tc(const msa_cache* c, const uint8_t* q, float so
                                   int n_seqs, int n_q_total, int n_splits, float* o_part,
                                   float* lse_part, cudaStream_t stream) {
   if (n_q_total == 0) return cudaSuccess;
-  static int s_n_sm[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static DeviceSetup setup;
+  int dev = 0, n_sm = 0;
+  cudaError_t e = setup.get(&dev, &n_sm, [](int) {
+    return cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)attn_smem_bytes(kMaxSeqs));
+  });
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (s_n_sm[dev] == 0) {
-    int n_sm = 0;
-    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn_smem_bytes(kMaxSeqs));
-    if (e != cudaSuccess) return e;
-    s_n_sm[dev] = n_sm;
-  }
   const int n_items = n_q_total * kKvHeads * n_splits;
   AttnParams ap{static_cast<const uint8_t*>(c->kv_pool), c->n_pages, q, sel, n_sel, block_table,
                 max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, n_splits, n_items,
                 softmax_scale / c->s_enc_k * kLog2e, 1.0f / (256.0f * c->s_enc_v), o_part,
-                lse_part, c->status};
-  const int grid = n_items < s_n_sm[dev] ? n_items : s_n_sm[dev];
+                lse_part, c->status, launch_settings().wait_ns};
+  const int grid = n_items < n_sm ? n_items : n_sm;
   return launch_pdl(sparse_attn_tc_kernel, dim3(grid), dim3(kThreads), attn_smem_bytes(n_seqs), stream, ap);
 }
 

@@ -9,6 +9,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/msa.h"
 
 namespace msa {
@@ -143,11 +146,19 @@ __device__ __forceinline__ uint2 dequant8(uint32_t w, uint2 t) {
 }
 
 // ---- mbarrier / TMA bulk copy / tcgen05 (inline PTX) --------------------------
-// Every wait is bounded: after kSpinLimit polls or kWaitLimitNs nanoseconds the
-// caller gets false and must abandon its loop (the kernel then reports
-// MSA_STATUS_TIMEOUT).
+// Every wait is bounded: after kSpinLimit polls or WaitCtl::limit_ns nanoseconds
+// the caller gets false and must abandon its loop (the kernel then reports
+// MSA_STATUS_TIMEOUT).  The limit is a kernel parameter (2 s unless the host
+// lowers it, see msa_debug_set_fault_injection).
 constexpr uint32_t kSpinLimit = 1u << 25;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+// Bounded-wait control of one CTA: the shared-memory flag its roles raise when
+// a wait gives up (the other roles then stop waiting too), and the time limit.
+struct WaitCtl {
+  volatile int* abort;
+  unsigned long long limit_ns;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -180,15 +191,79 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity; false on timeout or when another
-// role has already flagged *abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// role has already raised the abort flag (the flag is then raised too).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 1; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15) == 0 && (*abort || globaltimer_ns() - t0 > kWaitLimitNs)) break;
+    if ((i & 15) == 0 && (*w.abort || globaltimer_ns() - t0 > w.limit_ns)) break;
   }
-  *abort = 1;
+  *w.abort = 1;
+  return false;
+}
+// The same wait for teardown after an abort: it ignores the abort flag (the
+// CTA must still see its in-flight copies and MMAs land before it releases
+// shared or tensor memory) and is bounded by time and polls only.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15) == 0 && globaltimer_ns() - t0 > limit_ns) break;
+  }
+  return false;
+}
+
+// Grid-wide barrier of a launch whose CTAs are all co-resident (cooperative
+// launch), on one 64-bit word of global memory: generation in the high half,
+// arrival count in the low half.  Called by one thread per CTA; every CTA must
+// call it exactly once per barrier, also after an abort of its own (so the
+// count always reaches `target`).  The CTA that brings the count to `target`
+// returns the count to zero and advances the generation in one atomic, which
+// releases the others.  A waiter that times out withdraws its arrival (only
+// while the generation is unchanged and the count is below `target`, i.e. the
+// barrier cannot complete any more without it), raises *abort and returns
+// false; so the word is back at rest after every barrier, completed or not,
+// and later launches on the same word need no clearing.  `target` is the
+// number of CTAs (the fault-injection test passes one more, so that the wait
+// runs out).
+__device__ __forceinline__ bool grid_barrier(unsigned long long* word, uint32_t target, const WaitCtl& w) {
+  __threadfence();
+  const unsigned long long old = atomicAdd(word, 1ull);
+  const uint32_t gen = (uint32_t)(old >> 32);
+  if ((uint32_t)old + 1u == target) {
+    atomicAdd(word, (1ull << 32) - target);
+    __threadfence();
+    return true;
+  }
+  volatile unsigned long long* vw = word;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if ((uint32_t)(*vw >> 32) != gen) {
+      __threadfence();
+      return true;
+    }
+    if ((i & 63) == 63 && globaltimer_ns() - t0 > w.limit_ns) break;
+  }
+  unsigned long long cur = *vw;
+  while ((uint32_t)(cur >> 32) == gen && (uint32_t)cur < target) {
+    const unsigned long long prev = atomicCAS(word, cur, cur - 1);
+    if (prev == cur) {
+      *w.abort = 1;
+      return false;
+    }
+    cur = prev;
+  }
+  // completed while this CTA was giving up: wait (bounded) for the release
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if ((uint32_t)(*vw >> 32) != gen) {
+      __threadfence();
+      return true;
+    }
+    if ((i & 63) == 63 && globaltimer_ns() - t0 > 2 * w.limit_ns) break;
+  }
+  *w.abort = 1;
   return false;
 }
 __device__ __forceinline__ void fence_barrier_init() {
@@ -342,6 +417,49 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+// ---- host-side launch settings ----------------------------------------------------
+// Library-wide settings every launch reads (msa_debug_set_fault_injection):
+// the limit of one bounded wait, and test-only fault-injection flags.
+constexpr int kInjectBarrierTimeout = 1;  // the indexer's grid barrier waits for one CTA more than exist
+struct LaunchSettings {
+  unsigned long long wait_ns;
+  int inject;
+};
+LaunchSettings launch_settings();  // defined in msa_abi.cu
+
+// One-time per-device launch set-up (SM count, shared-memory opt-in) of one
+// kernel.  The set-up runs under a mutex, so first calls from several host
+// threads do not race, and the SM count is published only after it succeeded.
+struct DeviceSetup {
+  std::mutex mu;
+  std::atomic<int> n_sm[64] = {};
+
+  // The current device's SM count, running setup(dev) first if this is the
+  // first call on the device.
+  template <typename F>
+  cudaError_t get(int* dev_out, int* n_sm_out, F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int n = n_sm[dev].load(std::memory_order_acquire);
+    if (n == 0) {
+      std::lock_guard<std::mutex> lock(mu);
+      n = n_sm[dev].load(std::memory_order_relaxed);
+      if (n == 0) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = setup(dev);
+        if (e != cudaSuccess) return e;
+        n_sm[dev].store(n, std::memory_order_release);
+      }
+    }
+    *dev_out = dev;
+    *n_sm_out = n;
+    return cudaSuccess;
+  }
+};
 
 // ---- sequence metadata --------------------------------------------------------
 struct SeqInfo {

@@ -24,8 +24,6 @@
 // The index page is stored pre-swizzled (chunk c of token t at chunk c ^ (t&7)),
 // which is exactly the 128-byte-swizzled K-major operand layout, so a plain
 // bulk copy lands it ready for the tensor core.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace msa {
@@ -45,8 +43,10 @@ struct ScanParams {
   float* scores;  // [T][max_pages][4] partial block maxima
   int* sel;       // [T][17]
   int* n_sel;     // [T]
-  unsigned int* sync;  // grid barrier words: [0] arrivals, [1] generation
+  unsigned long long* sync;  // grid-barrier word (generation << 32 | arrivals)
   int* status;
+  unsigned long long wait_ns;  // limit of one bounded wait
+  int barrier_extra;           // test hook: arrivals the barrier waits for beyond the grid (0)
 };
 
 constexpr int kScanThreads = 320;  // 10 warps
@@ -61,7 +61,7 @@ constexpr int kOffB = kStages * kIdxPageBytes;  // 131,072
 constexpr int kOffBars = kOffB + 2 * kBBytes;   // 147,456
 constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccs + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kOffPrefix = kOffMisc + 32;  // misc: tmem slot, abort, page range [2] (int64)
+constexpr int kOffPrefix = kOffMisc + 32;  // misc: tmem slot, abort, page range [2] (int64), copies issued
 
 // After kOffPrefix, per sequence: weighted page prefix (int64, n_seqs + 1),
 // page prefix (n_seqs + 1), seq_lens (n_seqs), q_start_loc (n_seqs + 1).
@@ -357,32 +357,6 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
   }
 }
 
-// Grid-wide barrier of a cooperative launch (all CTAs co-resident), used once
-// per launch.  Each CTA fences its writes and counts itself in; the last one
-// bumps the generation word (releasing the others at once) and then returns
-// the counter to zero for the next launch.  Bounded: on timeout it raises
-// *abort and returns false.
-__device__ bool grid_barrier(unsigned int* sync, unsigned int n_ctas, volatile int* abort) {
-  __threadfence();
-  volatile unsigned int* gen = sync + 1;
-  const unsigned int g = *gen;
-  if (atomicAdd(sync, 1u) == n_ctas - 1) {
-    atomicAdd(sync + 1, 1u);
-    atomicExch(sync, 0u);
-    return true;
-  }
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (*gen != g) {
-      __threadfence();
-      return true;
-    }
-    if ((i & 63) == 63 && globaltimer_ns() - t0 > kWaitLimitNs) break;
-  }
-  *abort = 1;
-  return false;
-}
-
 __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -398,6 +372,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   const uint32_t done_bar = bar0 + 8 * (2 * kStages + 4 + 2 * kAccs);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  const WaitCtl wc{s_abort, p.wait_ns};
+  int* s_issued = reinterpret_cast<int*>(smem + kOffMisc + 24);
   long long* s_wpre = reinterpret_cast<long long*>(smem + kOffPrefix);
   int* s_prefix = reinterpret_cast<int*>(s_wpre + (p.n_seqs + 1));
   int* s_sl = s_prefix + (p.n_seqs + 1);
@@ -426,6 +402,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
     }
     mbar_init(done_bar, 1);
     *s_abort = 0;
+    *s_issued = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -520,7 +497,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
           const int st = it % kStages;
           int phys = __shfl_sync(0xffffffffu, cur, k);
           if (phys < 0 || phys >= p.n_pages) phys = 0;  // flagged by the epilogue
-          if (!mbar_wait(empty(st), ((it / kStages) & 1) ^ 1, s_abort)) return false;
+          if (!mbar_wait(empty(st), ((it / kStages) & 1) ^ 1, wc)) return false;
           if (lane == 0) {
             mbar_arrive_expect_tx(full(st), kIdxPageBytes);
             bulk_g2s(sbase + kOffStages + st * kIdxPageBytes, p.idx_pool + (size_t)phys * kIdxPageBytes,
@@ -531,17 +508,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
       }
       return true;
     });
-    if (*s_abort) {
-      // drain: no bulk copy may still be writing shared memory when the CTA exits
-      for (int k = max(0, it - kStages); k < it; ++k) mbar_wait(full(k % kStages), (k / kStages) & 1, s_abort);
-    }
+    if (lane == 0) *s_issued = it;  // copies issued, for the drain after an abort
   } else if (warp == 1) {
     // ---------------- MMA warp: B tile of each segment, then the MMAs ----------
     int it = 0, sg = 0;
     for_each_segment(p, s_prefix, s_sl, s_qsl, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
       const int slot = sg & 1;
       // the MMAs that read this slot two segments ago must be done
-      if (!mbar_wait(bempty(slot), ((sg >> 1) & 1) ^ 1, s_abort)) return false;
+      if (!mbar_wait(bempty(slot), ((sg >> 1) & 1) ^ 1, wc)) return false;
       // index queries of tokens j0..j0+nq-1 -> rows (token, head), 128-byte
       // swizzled K-major; rows up to the MMA's N are zero-padded
       const int n_rows = 16 * ((nq + 1) >> 1);
@@ -570,8 +544,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
         const uint64_t bdesc = umma_desc_sw128(sbase + kOffB + slot * kBBytes);
         for (int page = page0; page < page1; ++page, ++it) {
           const int st = it % kStages, acc = it % kAccs;
-          if (!mbar_wait(full(st), (it / kStages) & 1, s_abort)) { ok = false; break; }
-          if (!mbar_wait(tempty(acc), ((it / kAccs) & 1) ^ 1, s_abort)) { ok = false; break; }
+          if (!mbar_wait(full(st), (it / kStages) & 1, wc)) { ok = false; break; }
+          if (!mbar_wait(tempty(acc), ((it / kAccs) & 1) ^ 1, wc)) { ok = false; break; }
           tc_fence_after();
           const uint64_t adesc = umma_desc_sw128(sbase + kOffStages + st * kIdxPageBytes);
 #pragma unroll
@@ -587,13 +561,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
       ++sg;
       return ok;
     });
-    if (lane == 0 && *s_abort) {
-      // no tcgen05.mma may still be running when tensor memory is released
-      volatile int ignore = 0;
-      umma_commit(done_bar);
-      mbar_wait(done_bar, 0, &ignore);
-    }
-    __syncwarp();
   } else {
     // ---------------- epilogue: two sets of four warps, set = page parity ------
     // warps 2..5 and 6..9 -> TMEM lane quadrants 2,3,0,1; each warp writes the
@@ -619,7 +586,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
         const int phys = __shfl_sync(0xffffffffu, bt_cur, (page - page0) & 31);
         if ((it & 1) != set) continue;
         const int acc = it % kAccs;
-        if (!mbar_wait(tfull(acc), (it / kAccs) & 1, s_abort)) return false;
+        if (!mbar_wait(tfull(acc), (it / kAccs) & 1, wc)) return false;
         tc_fence_after();
         float m[kNqMax];
 #pragma unroll
@@ -660,6 +627,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   // ---------------- scan teardown ---------------------------------------------
   tc_fence_before();
   __syncthreads();
+  if (*s_abort) {
+    // after an abort (bounded waits that ignore the flag): no tcgen05.mma may
+    // still run when tensor memory is released, and no bulk copy may still be
+    // writing the ring when its shared memory is reused or the CTA exits
+    if (warp == 1 && lane == 0) {
+      umma_commit(done_bar);
+      mbar_wait_drain(done_bar, 0, p.wait_ns);
+    }
+    if (warp == 0 && lane == 0) {
+      const int n = *s_issued;
+      for (int k = max(0, n - kStages); k < n; ++k) mbar_wait_drain(full(k % kStages), (k / kStages) & 1, p.wait_ns);
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -672,7 +653,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   sm.tmax = reinterpret_cast<unsigned long long*>(smem + kOffB);                       // NT x 8 B
   sm.win = reinterpret_cast<int*>(smem + kOffB + 8 * kScanThreads);
   sm.misc = sm.win + kTopK;
-  if (tid == 0 && !*s_abort) grid_barrier(p.sync, gridDim.x, s_abort);
+  // every CTA counts itself in, also after an abort of its own, so that the
+  // barrier word is back at rest when the launch ends
+  if (tid == 0) grid_barrier(p.sync, gridDim.x + p.barrier_extra, wc);
   __syncthreads();
   if (!*s_abort) {
     for (int j = blockIdx.x; j < p.n_q_total; j += gridDim.x) {
@@ -690,32 +673,26 @@ cudaError_t launch_indexer_topk(const msa_cache* c, const uint8_t* q_idx, const 
                                 const int* q_start_loc, int n_seqs, int n_q_total, int* sel,
                                 int* n_sel, void* ws, cudaStream_t stream) {
   if (n_q_total == 0 || n_seqs == 0) return cudaSuccess;
+  // per-device launch set-up, done once (not a stream operation, so a later call
+  // may be captured into a CUDA graph)
+  static DeviceSetup setup;
+  int dev = 0, n_sm = 0;
+  cudaError_t e = setup.get(&dev, &n_sm, [](int) {
+    return cudaFuncSetAttribute(indexer_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)scan_smem_bytes(kMaxSeqs));
+  });
+  if (e != cudaSuccess) return e;
+  const LaunchSettings ls = launch_settings();
   // workspace: [0, 256) grid-barrier words, then the partial block maxima
-  unsigned int* sync = static_cast<unsigned int*>(ws);
+  unsigned long long* sync = static_cast<unsigned long long*>(ws);
   float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsSyncBytes);
   ScanParams sp{static_cast<const uint8_t*>(c->idx_pool), c->n_pages, q_idx, w, block_table,
                 max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, scores, sel, n_sel, sync,
-                c->status};
-  // per-device launch set-up, done once (not a stream operation, so a later call
-  // may be captured into a CUDA graph)
-  static int s_n_sm[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (s_n_sm[dev] == 0) {
-    int n_sm = 0;
-    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(indexer_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)scan_smem_bytes(kMaxSeqs));
-    if (e != cudaSuccess) return e;
-    s_n_sm[dev] = n_sm;
-  }
+                c->status, ls.wait_ns, (ls.inject & kInjectBarrierTimeout) ? 1 : 0};
   // one CTA per SM, all co-resident (cooperative launch): the top-k phase
   // waits for every CTA's scan at a grid barrier
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(s_n_sm[dev]);
+  cfg.gridDim = dim3(n_sm);
   cfg.blockDim = dim3(kScanThreads);
   cfg.dynamicSmemBytes = scan_smem_bytes(n_seqs);
   cfg.stream = stream;

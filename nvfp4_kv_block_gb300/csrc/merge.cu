@@ -11,11 +11,13 @@
 namespace msa {
 namespace {
 
-// out[j][h][:] = sum_s exp(lse_s - L) o_s; one CTA per (token, head), thread = channel.
+// out[j][h][:] = sum_s exp(lse_s - L) o_s and lse_out[j][h] = L; one CTA per
+// (token, head), thread = channel.
 __global__ void __launch_bounds__(kHeadDim) merge_kernel(const float* __restrict__ o_part,
                                                          const float* __restrict__ lse_part,
                                                          int n_heads, int n_splits,
-                                                         float* __restrict__ out) {
+                                                         float* __restrict__ out,
+                                                         float* __restrict__ lse_out) {
   const int row = blockIdx.x;  // j * n_heads + h
   const int j = row / n_heads, h = row % n_heads;
   const int ch = threadIdx.x;
@@ -33,6 +35,7 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(const float* __restrict
     }
   }
   out[(size_t)row * kHeadDim + ch] = den > 0.f ? num / den : 0.f;
+  if (lse_out && ch == 0) lse_out[row] = den > 0.f ? M + logf(den) : -INFINITY;
 }
 
 // Dequantised FP8 operands of one page in logical order, through the same
@@ -60,10 +63,10 @@ __global__ void __launch_bounds__(256) debug_fp8_page_kernel(const uint8_t* __re
 }  // namespace
 
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int n_q_total, int n_heads,
-                         int n_splits, float* out, cudaStream_t stream) {
+                         int n_splits, float* out, float* lse_out, cudaStream_t stream) {
   if (n_q_total == 0) return cudaSuccess;
   return launch_pdl(merge_kernel, dim3(n_q_total * n_heads), dim3(kHeadDim), 0, stream, o_part,
-                    lse_part, n_heads, n_splits, out);
+                    lse_part, n_heads, n_splits, out, lse_out);
 }
 
 cudaError_t launch_debug_fp8_page(const msa_cache* c, int64_t page, uint8_t* k8, uint8_t* v8,

@@ -16,8 +16,17 @@ cudaError_t launch_indexer_topk_noalloc(const msa_cache*, const uint8_t*, const 
 cudaError_t launch_sparse_attn_tc(const msa_cache*, const uint8_t*, float, const int*, const int*,
                                   const int*, int, const int*, const int*, int, int, int, float*,
                                   float*, cudaStream_t);
-cudaError_t launch_merge(const float*, const float*, int, int, int, float*, cudaStream_t);
+cudaError_t launch_merge(const float*, const float*, int, int, int, float*, float*, cudaStream_t);
 cudaError_t launch_debug_fp8_page(const msa_cache*, int64_t, uint8_t*, uint8_t*, cudaStream_t);
+
+namespace {
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_inject{0};
+}  // namespace
+
+LaunchSettings launch_settings() {
+  return LaunchSettings{g_wait_ns.load(std::memory_order_relaxed), g_inject.load(std::memory_order_relaxed)};
+}
 }  // namespace msa
 
 namespace {
@@ -126,11 +135,13 @@ int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q
 }
 
 int msa_merge_splits(const float* o_part, const float* lse_part, int32_t n_q_total,
-                     int32_t n_q_heads, int32_t n_splits, float* out, msa_stream_t stream) {
+                     int32_t n_q_heads, int32_t n_splits, float* out, float* lse,
+                     msa_stream_t stream) {
   if (n_q_total < 0 || n_q_heads <= 0 || n_splits < 1 || n_splits > msa::kMaxSplits)
     return MSA_ERR_INVALID_ARG;
+  if (n_q_heads > 1024 || n_q_total > 65535) return MSA_ERR_UNSUPPORTED_SHAPE;
   if (n_q_total > 0 && (!o_part || !lse_part || !out)) return MSA_ERR_INVALID_ARG;
-  return launched(msa::launch_merge(o_part, lse_part, n_q_total, n_q_heads, n_splits, out,
+  return launched(msa::launch_merge(o_part, lse_part, n_q_total, n_q_heads, n_splits, out, lse,
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -168,6 +179,14 @@ int msa_read_status(const msa_cache* cache, int32_t* host_out, msa_stream_t stre
   return cudaStreamSynchronize(s) == cudaSuccess ? MSA_OK : MSA_ERR_LAUNCH_FAILED;
 }
 
+int msa_debug_set_fault_injection(int32_t flags, uint64_t wait_limit_ns) {
+  if (flags & ~MSA_INJECT_BARRIER_TIMEOUT) return MSA_ERR_INVALID_ARG;
+  msa::g_wait_ns.store(wait_limit_ns ? (unsigned long long)wait_limit_ns : msa::kDefaultWaitLimitNs,
+                       std::memory_order_relaxed);
+  msa::g_inject.store(flags, std::memory_order_relaxed);
+  return MSA_OK;
+}
+
 const char* msa_status_string(int code) {
   switch (code) {
     case MSA_OK: return "ok";
@@ -180,6 +199,7 @@ const char* msa_status_string(int code) {
     case MSA_STATUS_BAD_PAGE: return "device: block table entry outside the pool";
     case MSA_STATUS_BAD_SEQ: return "device: inconsistent sequence lengths / query counts";
     case MSA_STATUS_BAD_SELECTION: return "device: selected block outside 0..r_j";
+    case MSA_STATUS_TIMEOUT: return "device: a bounded wait timed out; results invalid";
     default: return code > 0 ? "device: several status bits" : "unknown error";
   }
 }

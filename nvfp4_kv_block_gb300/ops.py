@@ -27,6 +27,8 @@ Q_HEADS = 16
 TOPK = 16
 KV_PAGE_BYTES = 73_728
 NOALLOC_SCRATCH_BYTES = 8 << 20  # MSA_INDEXER_NOALLOC_SCRATCH_BYTES
+INJECT_BARRIER_TIMEOUT = 0x1     # MSA_INJECT_BARRIER_TIMEOUT
+STATUS_BAD_SLOT, STATUS_BAD_PAGE, STATUS_BAD_SEQ, STATUS_BAD_SELECTION, STATUS_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
 IDX_PAGE_BYTES = 16_384
 
 ERRORS = {-1: "invalid argument", -2: "unsupported shape", -3: "workspace too small",
@@ -65,7 +67,8 @@ _SIGS = {
                                                 _P, _P, _P]),
     "msa_sparse_attn_decode": (ctypes.c_int, [_P, _P, _I32, ctypes.c_float, _P, _P, _P, _I32, _P,
                                               _P, _I32, _I32, _I32, _P, _P, _P]),
-    "msa_merge_splits": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P]),
+    "msa_merge_splits": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P]),
+    "msa_debug_set_fault_injection": (ctypes.c_int, [_I32, ctypes.c_uint64]),
     "msa_absmax": (ctypes.c_int, [_P, _I64, _P, _P]),
     "msa_encode_scale": (ctypes.c_float, [ctypes.c_float]),
     "msa_debug_fp8_page": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
@@ -217,13 +220,6 @@ def indexer_topk_noalloc(cache, q_idx, w, block_table, seq_lens, q_start_loc, se
     return sel, n_sel
 
 
-def block_scores_view(ws, n_q_total, max_pages):
-    """The fp32 block scores S[T, max_pages]: max of the four partial maxima per
-    block held in the indexer workspace (valid for blocks < r_j)."""
-    part = ws[256: 256 + n_q_total * max_pages * 16].view(torch.float32).view(n_q_total, max_pages, 4)
-    return part.amax(dim=-1)
-
-
 def sparse_attn_decode(cache, q, sel, n_sel, block_table, seq_lens, q_start_loc, n_splits,
                        softmax_scale=None, o_part=None, lse_part=None):
     T = q.shape[0]
@@ -247,14 +243,22 @@ def sparse_attn_decode(cache, q, sel, n_sel, block_table, seq_lens, q_start_loc,
     return o_part, lse_part
 
 
-def merge_splits(o_part, lse_part, out=None):
+def merge_splits(o_part, lse_part, out=None, lse=None):
+    """LSE merge of the splits: returns out [T, H, 128] (and fills lse [T, H] if given)."""
     T, S, H, D = o_part.shape
     if out is None:
         out = torch.empty((T, H, D), dtype=torch.float32, device=o_part.device)
+    lse_p = ctypes.c_void_p(None) if lse is None else _ptr(lse, torch.float32, "lse")
     _check(lib().msa_merge_splits(_ptr(o_part, torch.float32, "o_part"),
                                   _ptr(lse_part, torch.float32, "lse_part"), T, H, S,
-                                  _ptr(out, torch.float32, "out"), _stream()))
+                                  _ptr(out, torch.float32, "out"), lse_p, _stream()))
     return out
+
+
+def set_fault_injection(flags=0, wait_limit_ns=0):
+    """Test hook: wait limit of every later launch (0 = the 2 s default) and
+    fault-injection flags (INJECT_BARRIER_TIMEOUT); 0, 0 restores the defaults."""
+    _check(lib().msa_debug_set_fault_injection(int(flags), int(wait_limit_ns)))
 
 
 def debug_fp8_page(cache, page):

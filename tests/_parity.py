@@ -42,8 +42,14 @@ class OracleSide:
 
     def idx_bytes(self, b):
         if b not in self._idx:
-            x = self.wl.tokens(2, b, 0, self.wl.seq_lens[b], self.device).cpu().numpy()
-            self._idx[b] = formats.encode_e4m3(x.astype(np.float64))
+            if len(self._idx) >= 4:  # long contexts: keep a few sequences only
+                self._idx.pop(next(iter(self._idx)))
+            L = self.wl.seq_lens[b]
+            parts = []
+            for lo in range(0, L, 1 << 16):
+                x = self.wl.tokens(2, b, lo, min(L, lo + (1 << 16)), self.device).cpu().numpy()
+                parts.append(formats.encode_e4m3(x.astype(np.float64)))
+            self._idx[b] = np.concatenate(parts) if parts else np.zeros((0, 128), np.uint8)
         return self._idx[b]
 
     def kv_tokens(self, b, lo, hi):
@@ -89,6 +95,14 @@ class OracleSide:
         out, lse = oracle.attention.attend(self.q[j], k8, v8, softmax_scale, self.s_enc_k, self.s_enc_v)
         vmax = float(np.nanmax(np.abs(formats.decode_e4m3(v8)))) / float(self.s_enc_v)
         return out, lse, vmax
+
+
+def block_scores_from_workspace(ws, n_q_total, max_pages):
+    """Block scores S[T, max_pages] read from an indexer workspace: the
+    workspace holds four partial maxima per (token, block) after its first 256
+    bytes, and the block score is their max (valid for blocks < r_j)."""
+    part = ws[256: 256 + n_q_total * max_pages * 16].view(torch.float32).view(n_q_total, max_pages, 4)
+    return part.cpu().numpy().max(axis=-1)
 
 
 def selection_ok(gpu_sel, ora_sel, ora_scores, rel=1e-4):

@@ -77,9 +77,18 @@ def test_host_validation_needs_no_gpu(lib):
     assert lib.msa_sparse_attn_decode(ctypes.byref(c), *a) == -1
     a = list(attn); a[11] = 65
     assert lib.msa_sparse_attn_decode(ctypes.byref(c), *a) == -1
-    assert lib.msa_merge_splits(fake, fake, 1, 16, 0, fake, None) == -1
+    assert lib.msa_merge_splits(fake, fake, 1, 16, 0, fake, None, None) == -1
     assert lib.msa_debug_fp8_page(ctypes.byref(c), 5, fake, fake, None) == -1
     assert lib.msa_status_string(-3) == b"workspace too small"
+    assert lib.msa_status_string(0x10) == b"device: a bounded wait timed out; results invalid"
+    assert lib.msa_status_string(0x8) == b"device: selected block outside 0..r_j"
+    assert lib.msa_merge_splits(fake, fake, 1, 2000, 2, fake, None, None) == -2
+
+
+def test_fault_injection_settings_are_validated_on_the_host(lib):
+    assert lib.msa_debug_set_fault_injection(0x100, 0) == -1
+    assert lib.msa_debug_set_fault_injection(ops.INJECT_BARRIER_TIMEOUT, 1000) == 0
+    assert lib.msa_debug_set_fault_injection(0, 0) == 0
 
 
 def test_noalloc_entry_point_rejects_shapes_beyond_its_scratch(lib):
