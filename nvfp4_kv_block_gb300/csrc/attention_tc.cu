@@ -51,18 +51,19 @@ constexpr int kWarpConv0 = 4 + 4 * kSets;  // first conversion warp
 constexpr int kThreads = 32 * (kWarpConv0 + 8 * kConvSets);
 constexpr int kStages = 6;     // raw K and raw V ring depth
 constexpr int kRecs = 4;       // item records in flight
-constexpr int kK8Slots = 3;    // K8 buffers in tensor memory
-constexpr int kV8Tiles = 3;
+constexpr int kK8Slots = 4;    // K8 buffers in tensor memory (a power of two: slot = e & 3)
+constexpr int kV8Tiles = 4;    // V8 tiles in shared memory (a power of two)
 constexpr int kPO = 4;         // P tiles and O buffers
 // a V tile is reused only after the PV of page e - kV8Tiles completes the O
 // barrier of that page; with kV8Tiles <= kPO no later phase of that barrier can
 // complete before the V warps have seen it (that would need page e's V tile)
 static_assert(kV8Tiles <= kPO, "V tile reuse waits on the O barrier of page e - kV8Tiles");
+static_assert(kV8Tiles == kPO, "a V tile and the O buffer of its page share the slot index");
 constexpr int kHalfBytes = kHeadBytes / 2;  // 9,216: codes + scales of K (or V)
 constexpr int kTileBytes = 16384;           // [128 rows][128 B], swizzled
 constexpr int kOffV8 = 0;                                   // kV8Tiles V8 tiles
 constexpr int kOffQ = kV8Tiles * kTileBytes;                // kRecs x [16 rows][128 B]
-constexpr int kOffP = kOffQ + kRecs * 2048;                 // kPO x [16 rows][128 B]
+constexpr int kOffP = kOffQ + kRecs * 2048;                 // kPO x [128 tokens][16 B]
 constexpr int kOffKRaw = kOffP + kPO * 2048;                // kStages x 9,216
 constexpr int kOffVRaw = kOffKRaw + kStages * kHalfBytes;   // kStages x 9,216
 constexpr int kOffTab = kOffVRaw + kStages * kHalfBytes;    // uint2 [256]
@@ -122,7 +123,7 @@ struct AttnParams {
   int n_splits;
   int n_items;       // T * 4 * n_splits
   float scale_log2;  // softmax_scale / s_enc_k * log2(e)
-  float out_scale;   // 1 / (256 * s_enc_v)
+  float out_scale;   // 1 / s_enc_v (O and L both carry the factor 256 of P)
   float* o_part;     // [T][S][16][128]
   float* lse_part;   // [T][S][16]
   int* status;
@@ -297,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   } else if (warp == 1) {
     // ---------------- TMA producer: K and V halves of every page -------------------------
     if (lane == 0) {
-      int e = 0;
+      int e = 0, st = 0;
+      uint32_t ph = 0;  // ring stage of page e and its phase parity
       bool ok = true;
       for (int k = 0; ok && k < n_mine; ++k) {
         const int slot = k % kRecs;
@@ -306,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const int n = r->n_pg;
         const uint8_t* head = p.kv_pool + (size_t)r->kvh * kHeadBytes;
         for (int i = 0; i < n; ++i, ++e) {
-          const int st = e % kStages, ph = (e / kStages) & 1;
           const uint8_t* src = head + (size_t)r->phys[i] * kKvPageBytes;
           if (!mbar_wait(bar(kKrEmpty + st), ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(kKrFull + st), kHalfBytes);
@@ -316,6 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
           mbar_arrive_expect_tx(bar(kVrFull + st), kHalfBytes);
           bulk_g2s(sbase + kOffVRaw + st * kHalfBytes, src + kHalfBytes, kHalfBytes, bar(kVrFull + st));
           *s_issued_v = e + 1;
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1;
+          }
         }
         if (ok) mbar_arrive(bar(kRecEmpty + slot));
       }
@@ -334,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const int n = rec(slot)->n_pg;
         const uint64_t bdesc = umma_desc_sw128(sbase + kOffQ + slot * 2048);
         for (int i = 0; i < n; ++i, ++e) {
-          const int sl = e % kSets, ph = (e / kSets) & 1, ks = e % kK8Slots, kph = (e / kK8Slots) & 1;
+          const unsigned ue = e;
+          const int sl = ue % kSets, ph = (ue / kSets) & 1, ks = ue % kK8Slots, kph = (ue / kK8Slots) & 1;
           if (!mbar_wait(bar(kK8Full + ks), kph, wc) || !mbar_wait(bar(kSEmpty + sl), ph ^ 1, wc)) {
             ok = false;
             break;
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   } else if (warp == 3) {
     // ---------------- PV issuer ---------------------------------------------------------------
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_e4m3_amn(128, 16);
+      const uint32_t idesc = umma_idesc_e4m3_amn_bmn(128, 16);
       int e = 0;
       bool ok = true;
       for (int k = 0; ok && k < n_mine; ++k) {
@@ -366,20 +372,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const int n = rec(slot)->n_pg;
         mbar_arrive(bar(kRecEmpty + slot));  // nothing else of the record is needed
         for (int i = 0; i < n; ++i, ++e) {
-          const int v = e % kV8Tiles, vph = (e / kV8Tiles) & 1, po = e % kPO, pph = (e / kPO) & 1;
+          const unsigned ue = e;
+          const int v = ue % kV8Tiles, vph = (ue / kV8Tiles) & 1, po = ue % kPO, pph = (ue / kPO) & 1;
           if (!mbar_wait(bar(kV8Full + v), vph, wc) || !mbar_wait(bar(kPFull + po), pph, wc) ||
               !mbar_wait(bar(kOEmpty + po), pph ^ 1, wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t bdesc = umma_desc_sw128(sbase + kOffP + po * 2048);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            // A: V tile read MN-major; 32 tokens (4 swizzle atoms of 8 rows) per MMA
+            // A: V tile read MN-major; 32 tokens (4 swizzle atoms of 8 rows) per MMA.
+            // B: P tile, MN-major without swizzle: token t's 16 bytes at 16 t, so
+            // a core matrix (8 tokens x 16 bytes) is 128 contiguous bytes and the
+            // 32 tokens of one MMA are 512 bytes
             const uint64_t adesc =
                 umma_desc_sw128_lbo_sbo(sbase + kOffV8 + v * kTileBytes + kk * 4096, 1024, 1024);
-            umma_e4m3(tmem + kTmO + 16 * po, adesc, bdesc + 2 * kk, idesc, kk > 0);
+            const uint64_t bdesc = umma_desc_noswz_lbo_sbo(sbase + kOffP + po * 2048 + kk * 512, 128, 128);
+            umma_e4m3(tmem + kTmO + 16 * po, adesc, bdesc, idesc, kk > 0);
           }
           // one commit: page e's O is ready, and its V tile and P tile are free
           umma_commit(bar(kOFull + po));
@@ -413,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       v_off[ci][0] = tok * 128 + (((2 * c) ^ (tok & 7)) << 4);
       v_off[ci][1] = tok * 128 + (((2 * c + 1) ^ (tok & 7)) << 4);
     }
-    int e = 0;
+    int e = 0, st = 0;
+    uint32_t rph = 0;  // raw ring stage of page e and its phase parity
     bool ok = true;
     for (int k = 0; ok && k < n_mine; ++k) {
       const int slot = k % kRecs;
@@ -421,19 +432,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       const ItemRec* r = rec(slot);
       const int n = r->n_pg;
       for (int i = 0; i < n; ++i, ++e) {
-        const int st = e % kStages;
-        // output slot: K8 buffer e % kK8Slots (freed by its previous QK), V8 tile
-        // e % kV8Tiles (freed by the PV of page e - kV8Tiles, whose commit
-        // completes the O barrier of that page)
-        const int os = is_k ? e % kK8Slots : e % kV8Tiles;
-        bool got = warp_wait(bar(full0 + st), (e / kStages) & 1, wc);
+        // output slot: the K8 buffer e % kK8Slots (freed by its previous QK) or
+        // the V8 tile e % kV8Tiles (freed by the PV of page e - kV8Tiles, whose
+        // commit completes the O barrier of that page: O buffer e % kPO, the
+        // same index since kV8Tiles == kPO)
+        const unsigned ue = e;
+        const int os = is_k ? ue % kK8Slots : ue % kV8Tiles;
+        const uint32_t oph = is_k ? (ue / kK8Slots) & 1 : (ue / kV8Tiles) & 1;
+        bool got = warp_wait(bar(full0 + st), rph, wc);
         if (got) {
-          if (is_k) {
-            got = warp_wait(bar(kK8Empty + os), ((e / kK8Slots) & 1) ^ 1, wc);
-          } else if (e >= kV8Tiles) {
-            const int ev = e - kV8Tiles;
-            got = warp_wait(bar(kOFull + ev % kPO), (ev / kPO) & 1, wc);
-          }
+          if (is_k) got = warp_wait(bar(kK8Empty + os), oph ^ 1, wc);
+          else if (e >= kV8Tiles) got = warp_wait(bar(kOFull + os), oph ^ 1, wc);
         }
         if (!got) {
           ok = false;
@@ -474,6 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
           else mbar_arrive(bar(kV8Full + os));
           mbar_arrive(bar(empty0 + st));
         }
+        if (++st == kStages) {
+          st = 0;
+          rph ^= 1;
+        }
       }
       if (ok && lane == 0) mbar_arrive(bar(kRecEmpty + slot));
     }
@@ -505,8 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       }
       // O of page ef (relative to its page max) -> running state
       auto fold = [&](int ef) -> bool {
-        const int po = ef % kPO;
-        if (!warp_wait(bar(kOFull + po), (ef / kPO) & 1, wc)) return false;
+        const int po = (unsigned)ef % kPO;
+        if (!warp_wait(bar(kOFull + po), ((unsigned)ef / kPO) & 1, wc)) return false;
         tc_fence_after();
         float ov[8];
         tmem_ld8(trow + kTmO + 16 * po, ov);  // columns 0-3: hi terms, 4-7: remainders
@@ -519,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       };
       int e_prev = -1;
       for (int e = e0 + (set - e0 % kSets + kSets) % kSets; e < e0 + n; e += kSets) {
-        const int ph = (e / kSets) & 1;
+        const int ph = ((unsigned)e / kSets) & 1;
         bool good = warp_wait(bar(kSFull + set), ph, wc);
         float sv[4] = {0.f, 0.f, 0.f, 0.f};
         if (good) {
@@ -531,48 +544,52 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         }
         const bool live = row < r->valid[e - e0];
         float* rd = red + ph * 16;
-        float x[4];
+        float x[4], wm[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           x[h] = live ? sv[h] * p.scale_log2 : -INFINITY;
-          const float wm = warp_max(x[h]);
-          if (lane == 0) rd[quad * 4 + h] = wm;
+          wm[h] = warp_max_f32(x[h]);
         }
+        if (lane == 0) reinterpret_cast<float4*>(rd)[quad] = make_float4(wm[0], wm[1], wm[2], wm[3]);
         // page maxima complete; the set's four warps agree on whether to go on
         if (named_barrier_or(nb, 128, !good || !ok)) {
           ok = false;
           break;
         }
-        uint32_t p_hi = 0, p_lo = 0;
-        float a_cur[4], b_cur[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float mp = fmaxf(fmaxf(rd[h], rd[4 + h]), fmaxf(rd[8 + h], rd[12 + h]));
-          const float m_new = fmaxf(m_run[h], mp);
-          // m_new = -inf only while no key so far is visible (then everything is 0)
-          a_cur[h] = m_new == -INFINITY ? 1.f : fast_exp2(m_run[h] - m_new);
-          b_cur[h] = mp == -INFINITY ? 0.f : fast_exp2(mp - m_new);  // page scale -> running scale
-          const float pr = mp == -INFINITY ? 0.f : fast_exp2(x[h] - mp);  // relative to the page max
-          l_run[h] = l_run[h] * a_cur[h] + pr * b_cur[h];
-          m_run[h] = m_new;
-          const float v256 = pr * 256.f;
-          const uint32_t hi = f32_to_e4m3(v256);
-          const uint32_t lo = f32_to_e4m3(v256 - e4m3_to_f32(hi));
-          p_hi |= hi << (8 * h);
-          p_lo |= lo << (8 * h);
-        }
-        // P rows h (E4M3 of 256 p) and 4+h (E4M3 of the remainder), one byte per
-        // token: byte t of row n sits in chunk (t/16) ^ (n & 7)
-        const int po = e % kPO;
-        // P tile po is free once the PV of page e - kPO is done (its O barrier)
-        bool step_ok = warp_wait(bar(kOFull + po), ((e / kPO) & 1) ^ 1, wc);
-        if (step_ok) {
-          uint8_t* pt = smem + kOffP + po * 2048;
+        float a_cur[4], b_cur[4], v[4];
+        {
+          const float4 r0 = reinterpret_cast<const float4*>(rd)[0], r1 = reinterpret_cast<const float4*>(rd)[1];
+          const float4 r2 = reinterpret_cast<const float4*>(rd)[2], r3 = reinterpret_cast<const float4*>(rd)[3];
+          const float mps[4] = {fmaxf(fmaxf(r0.x, r1.x), fmaxf(r2.x, r3.x)), fmaxf(fmaxf(r0.y, r1.y), fmaxf(r2.y, r3.y)),
+                                fmaxf(fmaxf(r0.z, r1.z), fmaxf(r2.z, r3.z)), fmaxf(fmaxf(r0.w, r1.w), fmaxf(r2.w, r3.w))};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            pt[h * 128 + (((row >> 4) ^ h) << 4) + (row & 15)] = (uint8_t)(p_hi >> (8 * h));
-            pt[(4 + h) * 128 + (((row >> 4) ^ (4 + h)) << 4) + (row & 15)] = (uint8_t)(p_lo >> (8 * h));
+            const float mp = mps[h];
+            // one of the two rescale factors is 1: the running state (a) moves
+            // to the page max when it grows, else the page (b) to the running max
+            const bool grow = mp > m_run[h];
+            const float f = fast_exp2(grow ? m_run[h] - mp : mp - m_run[h]);
+            a_cur[h] = grow ? f : 1.f;
+            b_cur[h] = grow ? 1.f : (mp == -INFINITY ? 0.f : f);
+            m_run[h] = fmaxf(m_run[h], mp);
+            // 256 p relative to the page max (<= 256: exact range of E4M3)
+            v[h] = mp == -INFINITY ? 0.f : fast_exp2(x[h] - mp + 8.f);
+            l_run[h] = l_run[h] * a_cur[h] + v[h] * b_cur[h];
           }
+        }
+        // 256 p as two E4M3 terms: hi = E4M3(256 p), lo = E4M3(f16(256 p) - hi)
+        // (the f16 difference is exact: hi is within a factor of two of 256 p)
+        const uint32_t hi01 = cvt_e4m3x2_f32(v[1], v[0]), hi23 = cvt_e4m3x2_f32(v[3], v[2]);
+        const uint32_t lo01 = cvt_e4m3x2_f16x2(hsub2_u32(cvt_f16x2_f32(v[1], v[0]), cvt_f16x2_e4m3x2(hi01)));
+        const uint32_t lo23 = cvt_e4m3x2_f16x2(hsub2_u32(cvt_f16x2_f32(v[3], v[2]), cvt_f16x2_e4m3x2(hi23)));
+        // P tile row = token: bytes 0-3 hi terms of heads 0-3, 4-7 the remainders
+        // (bytes 8-15 stay zero: they pad N to 16)
+        const int po = (unsigned)e % kPO;
+        // P tile po is free once the PV of page e - kPO is done (its O barrier)
+        bool step_ok = warp_wait(bar(kOFull + po), (((unsigned)e / kPO) & 1) ^ 1, wc);
+        if (step_ok) {
+          *reinterpret_cast<uint2*>(smem + kOffP + po * 2048 + 16 * row) =
+              make_uint2(prmt(hi01, hi23, 0x5410u), prmt(lo01, lo23, 0x5410u));
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kPFull + po));
@@ -644,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
           }
           const bool nonempty = !aborted && got && Lm > 0.f;
           p.o_part[(row0 + h) * kHeadDim + row] = nonempty ? om / Lm * p.out_scale : 0.f;
-          if (row == 0) p.lse_part[row0 + h] = nonempty ? (m + log2f(Lm)) * kLn2 : -INFINITY;
+          if (row == 0) p.lse_part[row0 + h] = nonempty ? (m + log2f(Lm) - 8.f) * kLn2 : -INFINITY;
         }
         __syncwarp();
         if (lane == 0 && got) {
@@ -703,7 +720,7 @@ cudaError_t launch_sparse_attn_tc(const msa_cache* c, const uint8_t* q, float so
   const int n_items = n_q_total * kKvHeads * n_splits;
   AttnParams ap{static_cast<const uint8_t*>(c->kv_pool), c->n_pages, q, sel, n_sel, block_table,
                 max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, n_splits, n_items,
-                softmax_scale / c->s_enc_k * kLog2e, 1.0f / (256.0f * c->s_enc_v), o_part,
+                softmax_scale / c->s_enc_k * kLog2e, 1.0f / c->s_enc_v, o_part,
                 lse_part, c->status, launch_settings().wait_ns};
   const int grid = n_items < n_sm ? n_items : n_sm;
   return launch_pdl(sparse_attn_tc_kernel, dim3(grid), dim3(kThreads), attn_smem_bytes(n_seqs), stream, ap);

@@ -588,21 +588,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
         const int acc = it % kAccs;
         if (!mbar_wait(tfull(acc), (it / kAccs) & 1, wc)) return false;
         tc_fence_after();
-        float m[kNqMax];
-#pragma unroll
-        for (int c = 0; c < kNqMax / 2; ++c) {
-          if (2 * c < nq) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * quad) << 16) + acc * 64 + 16 * c, v);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              float sc = 0.f;
-#pragma unroll
-              for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[2 * c + u][h], fmaxf(v[8 * u + h], 0.f), sc);
-              m[2 * c + u] = sc;
-            }
-          }
-        }
+        // every column the page needs (16 per pair of query tokens: 2 x 8
+        // heads) in one load, then one wait, so the tensor-memory latency is
+        // paid once per page; the accumulator is released before the math
+        const uint32_t ta = tmem + ((uint32_t)(32 * quad) << 16) + acc * 64;
+        uint32_t v[64];
+        if (nq <= 2) tmem_ld32x32b_x16(ta, v);
+        else if (nq <= 4) tmem_ld32x32b_x32(ta, v);
+        else tmem_ld32x32b_x64(ta, v);
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty(acc));
@@ -610,7 +604,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
 #pragma unroll
         for (int jj = 0; jj < kNqMax; ++jj) {
           if (jj < nq) {
-            const float x = warp_max(m[jj]);
+            float sc = 0.f;
+#pragma unroll
+            for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[jj][h], fmaxf(__uint_as_float(v[8 * jj + h]), 0.f), sc);
+            const float x = warp_max_f32(sc);
             if (lane == jj) mine = x;
           }
         }
