@@ -251,12 +251,13 @@ def run_gpu(args, rank, world, local_rank):
     e2e = float(np.mean(e2e_ms))
 
     ins = time_insert(args, flush, stream, dev) if args.insert_tokens > 0 else None
+    pack = time_pack(args, flush, stream, dev) if args.pack_blocks > 0 else None
 
     if world > 1:
         ms, t_idx, e2e = max_over_ranks([ms, t_idx, e2e], dev)
     return dict(wl=wl, T=T, ms=ms, t_idx=t_idx, e2e=e2e, h2d=h2d, d2h=d2h, n_splits=n_splits,
                 idx_bytes=idx_bytes, kv_bytes=kv_bytes, alg_bytes=alg_bytes, clocks=clk,
-                launches=(3 if n_splits > 1 else 2) * args.steps, insert=ins)
+                launches=(3 if n_splits > 1 else 2) * args.steps, insert=ins, pack=pack)
 
 
 # Algorithmic bytes of inserting one token: fp32 K and V (2 x 4 x 128 x 4), the
@@ -264,6 +265,34 @@ def run_gpu(args, rank, world, local_rank):
 # and scales) and the FP8 index key (128 B) written.
 INSERT_READ_BYTES = 2 * 4 * 128 * 4 + 128 * 4 + 8
 INSERT_WRITE_BYTES = 576 + 128
+
+
+def time_pack(args, flush, stream, dev):
+    """Block-outer pack of a batch of blocks from several layers' pools into
+    contiguous rows (off the decode step; its own sub-measurement).  Algorithmic
+    bytes: every row byte read once from the pools and written once."""
+    n, layers = args.pack_blocks, args.pack_layers
+    caches = [ops.KVCache(n, 1.0, 1.0, dev) for _ in range(layers)]
+    g = torch.Generator(device=dev)
+    g.manual_seed(777)
+    pages = torch.randperm(n, generator=g, device=dev).to(torch.int32)
+    rows = torch.empty((n, ops.block_row_bytes(layers)), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        ops.pack_blocks(caches, pages, rows)
+    ts = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ops.pack_blocks(caches, pages, rows)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = float(np.mean(ts))
+    byts = 2 * rows.numel()
+    return {"kernel": "block_rows_kernel (msa_pack_blocks)", "blocks": n, "layers": layers,
+            "row_bytes": int(rows.shape[1]), "ms_per_launch": ms, "algorithmic_bytes_per_launch": byts,
+            "achieved_gbs": byts / (ms * 1e-3) / 1e9}
 
 
 def time_insert(args, flush, stream, dev):
@@ -368,6 +397,9 @@ def main():
     ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--insert-tokens", type=int, default=262144,
                     help="tokens of the timed quantise-insert sub-measurement (0: skip)")
+    ap.add_argument("--pack-blocks", type=int, default=2048,
+                    help="blocks of the timed block-outer pack sub-measurement (0: skip)")
+    ap.add_argument("--pack-layers", type=int, default=4)
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -436,6 +468,11 @@ def main():
         ins["frac"] = ins["achieved_gbs"] / peak
         ins["peak_kind"] = peak_kind
         line["quantize_insert"] = ins
+    if r["pack"] is not None:
+        pk = dict(r["pack"])
+        pk["frac"] = pk["achieved_gbs"] / peak
+        pk["peak_kind"] = peak_kind
+        line["pack_blocks"] = pk
     if not args.no_cpu_baseline:
         qps_cpu, cores, sample = oracle_sample(r["wl"], "cuda", args.cpu_budget)
         line["cpu_baseline"] = {"value": qps_cpu, "unit": "queries/s", "cores": cores, "kind": "oracle",

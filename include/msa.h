@@ -161,6 +161,47 @@ int msa_indexer_topk(const msa_cache* cache, const uint8_t* q_idx, const float* 
                      int32_t n_q_total, int32_t topk, int32_t* sel, int32_t* n_sel,
                      void* ws, size_t ws_bytes, msa_stream_t stream);
 
+/*
+ * Context-split indexer (blog, "Parallelize index work across context": each
+ * GPU scans a part of the context, the local candidates are exchanged, and
+ * merging them gives the final top-16 exactly: every block competes once,
+ * with the same score, in one part).  The two calls below let a caller run
+ * each part where its index pages live and merge anywhere.
+ *
+ * msa_indexer_topk_range: msa_indexer_topk restricted to the logical blocks
+ * [blk_lo, blk_hi) (0 <= blk_lo <= blk_hi) of every sequence: for query token
+ * j, only blocks i with blk_lo <= i < min(blk_hi, r_j) are scanned and
+ * compete; instead of sel / n_sel it writes
+ *   cand  uint64 [n_q_total][16] out: the local top-16 as keys, best first,
+ *         zero-padded (fewer than 16 blocks in the range: all of them).
+ *         key = (ordered(S) << 32) | (0xFFFFFFFF - block), where ordered(x)
+ *         is the fp32 bit pattern of x with the sign bit set for x >= +0 and
+ *         all bits inverted for x < 0; a larger key is a higher score, then
+ *         a lower block; 0 = no block.
+ * Only the block-table entries of the range are read.  Workspace and every
+ * other argument as msa_indexer_topk (its scores are written for the blocks
+ * of the range only).
+ *
+ * msa_indexer_merge_candidates: cand holds n_shards (1..64) such arrays,
+ * [n_shards][n_q_total][16], whose block ranges are disjoint; per query token
+ * the 16 largest non-zero keys win and sel / n_sel are written exactly as
+ * msa_indexer_topk writes them (winners ascending, then r_j, -1 padding;
+ * n_sel = winners + 1).  When the ranges tile [0, r_j) of every token, the
+ * result equals msa_indexer_topk's.  Status bits go to cache->status (the
+ * cache's pools are not read): MSA_STATUS_BAD_SEQ for an inconsistent
+ * sequence, MSA_STATUS_BAD_SELECTION for a key whose block is not below r_j.
+ * Launched as a programmatic dependent of the previous kernel in the stream.
+ */
+int msa_indexer_topk_range(const msa_cache* cache, const uint8_t* q_idx, const float* w,
+                           int32_t n_idx_heads, const int32_t* block_table, int32_t max_pages,
+                           const int32_t* seq_lens, const int32_t* q_start_loc, int32_t n_seqs,
+                           int32_t n_q_total, int32_t topk, int32_t blk_lo, int32_t blk_hi,
+                           uint64_t* cand, void* ws, size_t ws_bytes, msa_stream_t stream);
+int msa_indexer_merge_candidates(const msa_cache* cache, const uint64_t* cand, int32_t n_shards,
+                                 const int32_t* seq_lens, const int32_t* q_start_loc,
+                                 int32_t n_seqs, int32_t max_pages, int32_t n_q_total,
+                                 int32_t topk, int32_t* sel, int32_t* n_sel, msa_stream_t stream);
+
 /* Bytes of scratch msa_indexer_topk needs (a multiple of 256). */
 size_t msa_indexer_workspace_bytes(int32_t n_q_total, int32_t max_pages);
 
@@ -243,6 +284,32 @@ int msa_sparse_attn_decode(const msa_cache* cache, const uint8_t* q, int32_t n_q
 int msa_merge_splits(const float* o_part, const float* lse_part, int32_t n_q_total,
                      int32_t n_q_heads, int32_t n_splits, float* out, float* lse,
                      msa_stream_t stream);
+
+/*
+ * Block-outer transfer rows (blog, "AMD uses different conversion and
+ * communication mechanisms": a KV block kept as one contiguous row is moved in
+ * one read instead of one read per page).  The row of a block holds, for every
+ * layer l = 0 .. n_layers-1 in order, that layer's KV page (73,728 bytes, the
+ * format above) followed by its index page (16,384 bytes): 90,112 bytes per
+ * layer, msa_block_row_bytes(n_layers) per row.
+ *
+ *   layers   HOST array of n_layers caches (1 <= n_layers <= 128), one per
+ *            model layer; block i lives at the same physical page pages[i] in
+ *            every layer's pools.
+ *   pages    int32 [n_blocks] physical page of each block.  A page outside a
+ *            layer's pool sets MSA_STATUS_BAD_PAGE in layers[0].status and that
+ *            (block, layer) part of the row is left untouched.
+ *   rows     uint8 [n_blocks][msa_block_row_bytes(n_layers)], 16-byte aligned.
+ * msa_pack_blocks copies pages -> rows; msa_unpack_blocks copies rows -> pages
+ * (so a receiver may place a block at different page ids).  Rows and pages
+ * must not overlap; the pages listed in one unpack call must be distinct.
+ */
+int msa_pack_blocks(const msa_cache* layers, int32_t n_layers, const int32_t* pages,
+                    int32_t n_blocks, uint8_t* rows, msa_stream_t stream);
+int msa_unpack_blocks(const msa_cache* layers, int32_t n_layers, const uint8_t* rows,
+                      const int32_t* pages, int32_t n_blocks, msa_stream_t stream);
+/* Bytes of one block-outer row: n_layers * 90,112 (0 for n_layers <= 0). */
+size_t msa_block_row_bytes(int32_t n_layers);
 
 /*
  * Helpers for the per-tensor scale.  msa_absmax folds max|x[i]| over n fp32

@@ -36,6 +36,7 @@ constexpr int kOffKc = 0, kOffKs = 8192, kOffVc = 9216, kOffVs = 17408;
 __host__ __device__ __forceinline__ int code_chunk_pos(int c, int t) { return c ^ ((t >> 1) & 3); }
 constexpr int kMaxSeqs = 4096;
 constexpr int kMaxSplits = 64;
+constexpr int kMaxLayers = 128;  // layers one block-outer row may hold
 // Capacity of the file-scope scratch of msa_indexer_topk_noalloc.
 constexpr size_t kStaticScratchBytes = MSA_INDEXER_NOALLOC_SCRATCH_BYTES;
 

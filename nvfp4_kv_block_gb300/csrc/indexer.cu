@@ -47,6 +47,8 @@ struct ScanParams {
   int* status;
   unsigned long long wait_ns;  // limit of one bounded wait
   int barrier_extra;           // test hook: arrivals the barrier waits for beyond the grid (0)
+  int blk_lo, blk_hi;          // logical blocks scanned and selected from: [blk_lo, blk_hi)
+  unsigned long long* cand;    // range mode: [T][16] local top-16 keys instead of sel / n_sel
 };
 
 constexpr int kScanThreads = 320;  // 10 warps
@@ -76,9 +78,17 @@ __device__ __forceinline__ long long page_weight(int n_q) {
   return (long long)((n_q + kNqMax - 1) / kNqMax) * kPassCost + n_q;
 }
 
-// Pages to scan for sequence b: blocks 0..r_last-1, r_last = (seq_len-1)/128.
-__device__ __forceinline__ int scan_pages(const SeqInfo& s) {
+// Blocks a sequence's query tokens compete over: 0..r_last-1, r_last =
+// (seq_len-1)/128 (the recent block of its last token); scanned: their part
+// in [blk_lo, blk_hi), starting at block scan_first.
+__device__ __forceinline__ int r_last_of(const SeqInfo& s) {
   return (s.ok && s.seq_len > 0 && s.n_q > 0) ? (s.seq_len - 1) / kPageTokens : 0;
+}
+__device__ __forceinline__ int scan_first(const ScanParams& p, const SeqInfo& s) {
+  return min(p.blk_lo, r_last_of(s));
+}
+__device__ __forceinline__ int scan_pages(const ScanParams& p, const SeqInfo& s) {
+  return min(p.blk_hi, r_last_of(s)) - scan_first(p, s);
 }
 
 // Walks the segments (sequence, query-token group, page range) of the flattened
@@ -95,12 +105,14 @@ __device__ __forceinline__ void for_each_segment(const ScanParams& p, const int*
   while (pg < pg_end) {
     while (s_prefix[b + 1] <= pg) ++b;
     const SeqInfo s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
-    const int page0 = (int)(pg - s_prefix[b]);
-    const int page1 = (int)(min((long long)s_prefix[b + 1], pg_end) - s_prefix[b]);
+    // logical blocks of this piece (the sequence's scanned blocks start at scan_first)
+    const int lo_b = scan_first(p, s);
+    const int page0 = lo_b + (int)(pg - s_prefix[b]);
+    const int page1 = lo_b + (int)(min((long long)s_prefix[b + 1], pg_end) - s_prefix[b]);
     for (int j0 = 0; j0 < s.n_q; j0 += kNqMax) {
       if (!f(b, s, j0, min(kNqMax, s.n_q - j0), page0, page1)) return;
     }
-    pg = s_prefix[b] + page1;
+    pg = s_prefix[b] + (page1 - lo_b);
     ++b;
   }
 }
@@ -124,8 +136,8 @@ struct TopkSmem {
   float* sc;                 // [kTopkStage]
   unsigned long long* cand;  // [kMaxCand]
   unsigned long long* tmax;  // [NT] per-warp survivors, theta, reduction scratch
-  int* win;                  // [16]
-  int* misc;                 // [0] n_cand
+  unsigned long long* win;   // [16] winning keys by rank
+  int* misc;                 // [0] n_cand, [1..] per-warp counts
 };
 
 // Sequence of query token j (-1 if none): the b with q_start_loc[b] <= j <
@@ -142,70 +154,103 @@ __device__ __forceinline__ int token_sequence(const int* s_qsl, int n_seqs, int 
   return (s_qsl[lo] <= j && j < s_qsl[lo + 1]) ? lo : -1;
 }
 
+__device__ __forceinline__ unsigned long long make_key(float sc, int blk) {
+  return ((unsigned long long)ordered_bits(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
+}
+__device__ __forceinline__ int key_block(unsigned long long k) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFu));
+}
+
+// Top-16 of query token j over its competing blocks [lo, e), e = min(blk_hi,
+// r_j), lo = min(blk_lo, e).  Final mode (p.cand == nullptr; the whole range
+// [0, r_j)): sel = the winners ascending, then r_j.  Range mode: the winners'
+// keys in rank order (best first), zero-padded, into p.cand[j][0..15].
 template <int NT>
 __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const int* s_qsl,
                              const TopkSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31;
+  const bool range_mode = p.cand != nullptr;
   const int b = token_sequence(s_qsl, p.n_seqs, j);
   SeqInfo s{0, 0, 0, false};
   if (b >= 0) s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
   int* out = p.sel + (size_t)j * kSelStride;
+  unsigned long long* kout = range_mode ? p.cand + (size_t)j * kTopK : nullptr;
   if (b < 0 || !s.ok) {
     if (tid == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
-    if (tid < kSelStride) out[tid] = -1;
-    if (tid == 0) p.n_sel[j] = 0;
+    if (range_mode) {
+      if (tid < kTopK) kout[tid] = 0ull;
+    } else {
+      if (tid < kSelStride) out[tid] = -1;
+      if (tid == 0) p.n_sel[j] = 0;
+    }
     return;
   }
   const int pos = s.seq_len - s.n_q + (j - s.q0);
   const int r = pos / kPageTokens;
-  if (r <= kTopK) {
-    if (tid < kSelStride) out[tid] = tid <= r ? tid : -1;
-    if (tid == 0) p.n_sel[j] = r + 1;
+  const int e = min(p.blk_hi, r), lo = min(p.blk_lo, e);
+  const int n = e - lo;  // competing blocks lo .. e-1
+  // block score = max of the four partial maxima (written by other CTAs: read
+  // through L2)
+  const float4* row = reinterpret_cast<const float4*>(p.scores + (size_t)j * p.max_pages * 4) + lo;
+  if (n <= kTopK) {
+    if (range_mode) {
+      // every block of the range wins; warp 0 ranks their keys, best first
+      if (tid < 32) {
+        unsigned long long k = 0ull;
+        if (tid < n) {
+          const float4 v = __ldcg(row + tid);
+          k = make_key(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)), lo + tid);
+        }
+        int rk = 0;
+#pragma unroll
+        for (int t = 0; t < kTopK; ++t) rk += __shfl_sync(0xffffffffu, k, t) > k;
+        if (tid < n) kout[rk] = k;
+        else if (tid < kTopK) kout[tid] = 0ull;
+      }
+    } else {
+      if (tid < kSelStride) out[tid] = tid <= r ? tid : -1;
+      if (tid == 0) p.n_sel[j] = r + 1;
+    }
     return;
   }
-  // block score = max of the four partial maxima (written by other CTAs: read
-  // through L2).  Up to kRegKeys blocks per thread the keys live in registers
-  // (all loads in flight at once, no shared-memory staging); longer rows are
-  // staged in shared memory, or read from L2 each time beyond kTopkStage.
+  // Up to kRegKeys blocks per thread the keys live in registers (all loads in
+  // flight at once, no shared-memory staging); longer rows are staged in
+  // shared memory, or read from L2 each time beyond kTopkStage.
   constexpr int kRegKeys = 16;
-  const float4* row = reinterpret_cast<const float4*>(p.scores + (size_t)j * p.max_pages * 4);
-  const bool in_regs = r <= kRegKeys * NT;
-  const bool staged = !in_regs && r <= kTopkStage;
-  auto make_key = [](float sc, int blk) -> unsigned long long {
-    return ((unsigned long long)ordered_bits(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
-  };
-  auto score = [&](int blk) -> float {
-    if (staged) return sm.sc[blk];
-    const float4 v = __ldcg(row + blk);
+  const bool in_regs = n <= kRegKeys * NT;
+  const bool staged = !in_regs && n <= kTopkStage;
+  auto score = [&](int i) -> float {
+    if (staged) return sm.sc[i];
+    const float4 v = __ldcg(row + i);
     return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
   };
-  auto key = [&](int blk) -> unsigned long long { return make_key(score(blk), blk); };
-  unsigned long long kr[kRegKeys];  // block tid + u NT; 0 = no block (every real key is > 0)
+  auto key = [&](int i) -> unsigned long long { return make_key(score(i), lo + i); };
+  unsigned long long kr[kRegKeys];  // block lo + tid + u NT; 0 = no block (every real key is > 0)
   if (in_regs) {
     float4 v4[kRegKeys];
 #pragma unroll
     for (int u = 0; u < kRegKeys; ++u) {
-      const int blk = tid + u * NT;
-      v4[u] = blk < r ? __ldcg(row + blk) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const int i = tid + u * NT;
+      v4[u] = i < n ? __ldcg(row + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kRegKeys; ++u) {
-      const int blk = tid + u * NT;
-      kr[u] = blk < r ? make_key(fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w)), blk) : 0ull;
+      const int i = tid + u * NT;
+      kr[u] = i < n ? make_key(fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w)), lo + i) : 0ull;
     }
   } else if (staged) {
     // batches of 8 loads in flight per thread, then the stores
-    for (int base = tid; base < r; base += 8 * NT) {
+    for (int base = tid; base < n; base += 8 * NT) {
       float4 v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int blk = base + u * NT;
-        v[u] = blk < r ? __ldcg(row + blk) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int i = base + u * NT;
+        v[u] = i < n ? __ldcg(row + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int blk = base + u * NT;
-        if (blk < r) sm.sc[blk] = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
+        const int i = base + u * NT;
+        if (i < n) sm.sc[i] = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
       }
     }
   }
@@ -217,7 +262,7 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
   // at or above x, then x <= the 16th largest key; so the (16/m)-th largest of
   // the warps' m-th largest maxima (as a key with the block bits clear) is a
   // lower bound of the 16th largest key, and theta is the largest of these four
-  // bounds.  Every winner is then a candidate.  (r > 16 here; real keys are
+  // bounds.  Every winner is then a candidate.  (n > 16 here; real keys are
   // distinct and > 0, a missing key counts as 0.)
   constexpr int kNW = NT / 32;
   unsigned long long vmax = 0;
@@ -225,7 +270,7 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
 #pragma unroll
     for (int u = 0; u < kRegKeys; ++u) vmax = umax64(vmax, kr[u]);
   } else {
-    for (int blk = tid; blk < r; blk += NT) vmax = umax64(vmax, key(blk));
+    for (int i = tid; i < n; i += NT) vmax = umax64(vmax, key(i));
   }
   uint32_t v = (uint32_t)(vmax >> 32);
 #pragma unroll
@@ -261,7 +306,7 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
 #pragma unroll
     for (int u = 0; u < kRegKeys; ++u) cnt += kr[u] >= theta;
   } else {
-    for (int blk = tid; blk < r; blk += NT) cnt += key(blk) >= theta;
+    for (int i = tid; i < n; i += NT) cnt += key(i) >= theta;
   }
   int incl = cnt;
 #pragma unroll
@@ -288,8 +333,8 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
         }
       }
     } else {
-      for (int blk = tid; blk < r; blk += NT) {
-        const unsigned long long k = key(blk);
+      for (int i = tid; i < n; i += NT) {
+        const unsigned long long k = key(i);
         if (k >= theta) {
           if (at < kMaxCand) sm.cand[at] = k;
           ++at;
@@ -313,7 +358,7 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
         const ulonglong2 v = c2[i];
         rk += (v.x > k) + (v.y > k);
       }
-      if (rk < kTopK) sm.win[rk] = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFu));
+      if (rk < kTopK) sm.win[rk] = k;
     }
   } else {
     // too many candidates for the buffer (adversarial score layouts): 16 rounds
@@ -326,8 +371,8 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
         for (int u = 0; u < kRegKeys; ++u)
           if (kr[u] < bound) best = umax64(best, kr[u]);
       } else {
-        for (int blk = tid; blk < r; blk += NT) {
-          const unsigned long long kk = key(blk);
+        for (int i = tid; i < n; i += NT) {
+          const unsigned long long kk = key(i);
           if (kk < bound) best = umax64(best, kk);
         }
       }
@@ -336,7 +381,7 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
       if (tid == 0) {
         for (int i = 1; i < NT; ++i) best = umax64(best, sm.tmax[i]);
         sm.tmax[0] = best;
-        sm.win[k] = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+        sm.win[k] = best;
       }
       __syncthreads();
       bound = sm.tmax[0];
@@ -344,11 +389,15 @@ __device__ void select_token(const ScanParams& p, int j, const int* s_sl, const 
     }
   }
   __syncthreads();
+  if (range_mode) {
+    if (tid < kTopK) kout[tid] = sm.win[tid];
+    return;
+  }
   if (tid < kTopK) {
-    const int blk = sm.win[tid];
+    const int blk = key_block(sm.win[tid]);
     int at = 0;
 #pragma unroll
-    for (int i = 0; i < kTopK; ++i) at += sm.win[i] < blk;
+    for (int i = 0; i < kTopK; ++i) at += key_block(sm.win[i]) < blk;
     out[at] = blk;
   }
   if (tid == 0) {
@@ -414,7 +463,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
     for (int b = b0; b < b1; ++b) {
       const SeqInfo s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
       if (!s.ok && blockIdx.x == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
-      const int pages = scan_pages(s);
+      const int pages = scan_pages(p, s);
       lp += pages;
       lw += pages * page_weight(s.n_q);
     }
@@ -444,7 +493,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
       s_prefix[b] = (int)rp;
       s_wpre[b] = rw;
       const SeqInfo s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
-      const int pages = scan_pages(s);
+      const int pages = scan_pages(p, s);
       rp += pages;
       rw += pages * page_weight(s.n_q);
     }
@@ -648,8 +697,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   sm.sc = reinterpret_cast<float*>(smem + kOffStages);                                 // 64 KB
   sm.cand = reinterpret_cast<unsigned long long*>(smem + kOffStages + 4 * kTopkStage);  // 16 KB
   sm.tmax = reinterpret_cast<unsigned long long*>(smem + kOffB);                       // NT x 8 B
-  sm.win = reinterpret_cast<int*>(smem + kOffB + 8 * kScanThreads);
-  sm.misc = sm.win + kTopK;
+  sm.win = reinterpret_cast<unsigned long long*>(smem + kOffB + 8 * kScanThreads);
+  sm.misc = reinterpret_cast<int*>(sm.win + kTopK);
   // every CTA counts itself in, also after an abort of its own, so that the
   // barrier word is back at rest when the launch ends
   if (tid == 0) grid_barrier(p.sync, gridDim.x + p.barrier_extra, wc);
@@ -668,7 +717,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
 cudaError_t launch_indexer_topk(const msa_cache* c, const uint8_t* q_idx, const float* w,
                                 const int* block_table, int max_pages, const int* seq_lens,
                                 const int* q_start_loc, int n_seqs, int n_q_total, int* sel,
-                                int* n_sel, void* ws, cudaStream_t stream) {
+                                int* n_sel, void* ws, int blk_lo, int blk_hi,
+                                unsigned long long* cand, cudaStream_t stream) {
   if (n_q_total == 0 || n_seqs == 0) return cudaSuccess;
   // per-device launch set-up, done once (not a stream operation, so a later call
   // may be captured into a CUDA graph)
@@ -685,7 +735,8 @@ cudaError_t launch_indexer_topk(const msa_cache* c, const uint8_t* q_idx, const 
   float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsSyncBytes);
   ScanParams sp{static_cast<const uint8_t*>(c->idx_pool), c->n_pages, q_idx, w, block_table,
                 max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, scores, sel, n_sel, sync,
-                c->status, ls.wait_ns, (ls.inject & kInjectBarrierTimeout) ? 1 : 0};
+                c->status, ls.wait_ns, (ls.inject & kInjectBarrierTimeout) ? 1 : 0, blk_lo, blk_hi,
+                cand};
   // one CTA per SM, all co-resident (cooperative launch): the top-k phase
   // waits for every CTA's scan at a grid barrier
   cudaLaunchConfig_t cfg = {};
@@ -737,7 +788,8 @@ cudaError_t launch_indexer_topk_noalloc(const msa_cache* c, const uint8_t* q_idx
     scratch = g_static_ptr[dev];
   }
   return launch_indexer_topk(c, q_idx, w, block_table, max_pages, seq_lens, q_start_loc, n_seqs,
-                             n_q_total, sel, n_sel, static_cast<void*>(scratch), stream);
+                             n_q_total, sel, n_sel, static_cast<void*>(scratch), 0, 0x7FFFFFFF,
+                             nullptr, stream);
 }
 
 }  // namespace msa

@@ -60,7 +60,82 @@ __global__ void __launch_bounds__(256) debug_fp8_page_kernel(const uint8_t* __re
   *reinterpret_cast<uint4*>(dst) = make_uint4(d0.x, d0.y, d1.x, d1.y);
 }
 
+// Merge of the indexer's per-shard candidates (blog, "Parallelize index work
+// across context": each GPU scans part of the context, the local candidates
+// are exchanged, and a merge gives the final top-16 -- exactly the selection
+// of one scan over everything, because every block competes once, with the
+// same score, in exactly one shard).  One warp per query token: its
+// n_shards x 16 keys are staged in shared memory and ranked by counting (keys
+// are unique: the block id is part of the key; zero = empty); the 16 best
+// non-empty keys win, output in ascending block order, then the recent block.
+constexpr int kMergeWarps = 4;
+constexpr int kMaxShards = 64;
+
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_candidates_kernel(
+    const unsigned long long* __restrict__ cand, int n_shards, const int* __restrict__ seq_lens,
+    const int* __restrict__ q_start_loc, int n_seqs, int max_pages, int n_q_total, int* sel,
+    int* n_sel, int* status) {
+  __shared__ unsigned long long s_keys[kMergeWarps][kMaxShards * kTopK];
+  __shared__ unsigned long long s_win[kMergeWarps][kTopK];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int j = blockIdx.x * kMergeWarps + wid;
+  pdl_wait();  // candidates come from the range scans
+  if (j >= n_q_total) return;
+  unsigned long long* keys = s_keys[wid];
+  unsigned long long* win = s_win[wid];
+  int* out = sel + (size_t)j * kSelStride;
+  const int b = find_seq(q_start_loc, n_seqs, j);
+  const SeqInfo s = load_seq(b, seq_lens, q_start_loc, max_pages, n_q_total);
+  if (!(s.ok && s.q0 <= j && j < s.q0 + s.n_q)) {
+    if (lane == 0) set_status(status, MSA_STATUS_BAD_SEQ);
+    if (lane < kSelStride) out[lane] = -1;
+    if (lane == 0) n_sel[j] = 0;
+    return;
+  }
+  const int r = (s.seq_len - s.n_q + (j - s.q0)) / kPageTokens;
+  const int nk = n_shards * kTopK;
+  for (int i = lane; i < nk; i += 32)
+    keys[i] = cand[((size_t)(i / kTopK) * n_q_total + j) * kTopK + (i % kTopK)];
+  if (lane < kTopK) win[lane] = 0ull;
+  __syncwarp();
+  for (int i = lane; i < nk; i += 32) {
+    const unsigned long long k = keys[i];
+    if (k == 0ull) continue;
+    int rk = 0;
+    for (int t = 0; t < nk; ++t) rk += keys[t] > k;
+    if (rk < kTopK) win[rk] = k;
+  }
+  __syncwarp();
+  // winners are ranks 0 .. nw-1 (ranks of distinct non-zero keys are distinct)
+  const unsigned long long mine = lane < kTopK ? win[lane] : 0ull;
+  const int nw = __popc(__ballot_sync(0xffffffffu, mine != 0ull));
+  const int blk = (int)(0xFFFFFFFFu - (uint32_t)(mine & 0xFFFFFFFFu));
+  bool bad = false;
+  if (mine != 0ull) {
+    bad = blk < 0 || blk >= r;
+    int at = 0;
+    for (int t = 0; t < nw; ++t) {
+      const unsigned long long o = win[t];
+      at += (int)(0xFFFFFFFFu - (uint32_t)(o & 0xFFFFFFFFu)) < blk;
+    }
+    out[at] = blk;
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MSA_STATUS_BAD_SELECTION);
+  if (lane == nw) out[nw] = r;
+  if (lane > nw && lane < kSelStride) out[lane] = -1;
+  if (lane == 0) n_sel[j] = nw + 1;
+}
+
 }  // namespace
+
+cudaError_t launch_merge_candidates(const unsigned long long* cand, int n_shards, const int* seq_lens,
+                                    const int* q_start_loc, int n_seqs, int max_pages, int n_q_total,
+                                    int* sel, int* n_sel, int* status, cudaStream_t stream) {
+  if (n_q_total == 0) return cudaSuccess;
+  return launch_pdl(merge_candidates_kernel, dim3((n_q_total + kMergeWarps - 1) / kMergeWarps),
+                    dim3(32 * kMergeWarps), 0, stream, cand, n_shards, seq_lens, q_start_loc, n_seqs,
+                    max_pages, n_q_total, sel, n_sel, status);
+}
 
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int n_q_total, int n_heads,
                          int n_splits, float* out, float* lse_out, cudaStream_t stream) {

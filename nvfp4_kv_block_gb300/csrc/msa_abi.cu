@@ -9,7 +9,10 @@ cudaError_t launch_quantize_insert(const msa_cache*, const float*, const float*,
                                    const int64_t*, int, cudaStream_t);
 cudaError_t launch_absmax(const float*, int64_t, float*, cudaStream_t);
 cudaError_t launch_indexer_topk(const msa_cache*, const uint8_t*, const float*, const int*, int,
-                                const int*, const int*, int, int, int*, int*, void*, cudaStream_t);
+                                const int*, const int*, int, int, int*, int*, void*, int, int,
+                                unsigned long long*, cudaStream_t);
+cudaError_t launch_merge_candidates(const unsigned long long*, int, const int*, const int*, int, int,
+                                    int, int*, int*, int*, cudaStream_t);
 cudaError_t launch_indexer_topk_noalloc(const msa_cache*, const uint8_t*, const float*, const int*,
                                         int, const int*, const int*, int, int, int*, int*,
                                         cudaStream_t);
@@ -18,6 +21,7 @@ cudaError_t launch_sparse_attn_tc(const msa_cache*, const uint8_t*, float, const
                                   float*, cudaStream_t);
 cudaError_t launch_merge(const float*, const float*, int, int, int, float*, float*, cudaStream_t);
 cudaError_t launch_debug_fp8_page(const msa_cache*, int64_t, uint8_t*, uint8_t*, cudaStream_t);
+cudaError_t launch_block_rows(const msa_cache*, int, const int*, int, uint8_t*, bool, cudaStream_t);
 
 namespace {
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitLimitNs};
@@ -87,8 +91,53 @@ int msa_indexer_topk(const msa_cache* cache, const uint8_t* q_idx, const float* 
   if (ws_bytes < msa_indexer_workspace_bytes(n_q_total, max_pages))
     return MSA_ERR_WORKSPACE_TOO_SMALL;
   return launched(msa::launch_indexer_topk(cache, q_idx, w, block_table, max_pages, seq_lens,
-                                           q_start_loc, n_seqs, n_q_total, sel, n_sel, ws,
+                                           q_start_loc, n_seqs, n_q_total, sel, n_sel, ws, 0,
+                                           0x7FFFFFFF, nullptr,
                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_indexer_topk_range(const msa_cache* cache, const uint8_t* q_idx, const float* w,
+                           int32_t n_idx_heads, const int32_t* block_table, int32_t max_pages,
+                           const int32_t* seq_lens, const int32_t* q_start_loc, int32_t n_seqs,
+                           int32_t n_q_total, int32_t topk, int32_t blk_lo, int32_t blk_hi,
+                           uint64_t* cand, void* ws, size_t ws_bytes, msa_stream_t stream) {
+  if (int rc = check_cache(cache)) return rc;
+  if (n_idx_heads != msa::kIdxHeads || topk != msa::kTopK) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_seqs < 0 || n_q_total < 0 || max_pages <= 0 || blk_lo < 0 || blk_hi < blk_lo)
+    return MSA_ERR_INVALID_ARG;
+  if (n_seqs > msa::kMaxSeqs || max_pages > kMaxPagesPerSeq) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_q_total > 0 && (!q_idx || !w || !block_table || !seq_lens || !q_start_loc || !cand ||
+                        !ws || n_seqs == 0))
+    return MSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_idx) & 15) || (reinterpret_cast<uintptr_t>(w) & 7) ||
+      (reinterpret_cast<uintptr_t>(ws) & 15) || (reinterpret_cast<uintptr_t>(cand) & 7))
+    return MSA_ERR_INVALID_ARG;
+  if (ws_bytes < msa_indexer_workspace_bytes(n_q_total, max_pages))
+    return MSA_ERR_WORKSPACE_TOO_SMALL;
+  // sel / n_sel are not written in range mode; the candidates are
+  return launched(msa::launch_indexer_topk(cache, q_idx, w, block_table, max_pages, seq_lens,
+                                           q_start_loc, n_seqs, n_q_total, nullptr, nullptr, ws,
+                                           blk_lo, blk_hi,
+                                           reinterpret_cast<unsigned long long*>(cand),
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_indexer_merge_candidates(const msa_cache* cache, const uint64_t* cand, int32_t n_shards,
+                                 const int32_t* seq_lens, const int32_t* q_start_loc,
+                                 int32_t n_seqs, int32_t max_pages, int32_t n_q_total,
+                                 int32_t topk, int32_t* sel, int32_t* n_sel, msa_stream_t stream) {
+  if (!cache) return MSA_ERR_INVALID_ARG;
+  if (topk != msa::kTopK) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_shards < 1 || n_shards > 64 || n_seqs < 0 || n_q_total < 0 || max_pages <= 0)
+    return MSA_ERR_INVALID_ARG;
+  if (n_seqs > msa::kMaxSeqs || max_pages > kMaxPagesPerSeq) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_q_total > 0 && (!cand || !seq_lens || !q_start_loc || !sel || !n_sel || n_seqs == 0))
+    return MSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(cand) & 7) return MSA_ERR_INVALID_ARG;
+  return launched(msa::launch_merge_candidates(reinterpret_cast<const unsigned long long*>(cand),
+                                               n_shards, seq_lens, q_start_loc, n_seqs, max_pages,
+                                               n_q_total, sel, n_sel, cache->status,
+                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int msa_indexer_topk_noalloc(const msa_cache* cache, const uint8_t* q_idx, const float* w,
@@ -177,6 +226,35 @@ int msa_read_status(const msa_cache* cache, int32_t* host_out, msa_stream_t stre
       cudaSuccess)
     return MSA_ERR_LAUNCH_FAILED;
   return cudaStreamSynchronize(s) == cudaSuccess ? MSA_OK : MSA_ERR_LAUNCH_FAILED;
+}
+
+size_t msa_block_row_bytes(int32_t n_layers) {
+  return n_layers > 0 ? (size_t)n_layers * (msa::kKvPageBytes + msa::kIdxPageBytes) : 0;
+}
+
+static int block_rows(const msa_cache* layers, int32_t n_layers, const int32_t* pages,
+                      int32_t n_blocks, uint8_t* rows, bool pack, msa_stream_t stream) {
+  if (!layers || n_layers <= 0 || n_blocks < 0) return MSA_ERR_INVALID_ARG;
+  if (n_layers > msa::kMaxLayers) return MSA_ERR_UNSUPPORTED_SHAPE;
+  for (int l = 0; l < n_layers; ++l) {
+    if (int rc = check_cache(&layers[l])) return rc;
+    if ((reinterpret_cast<uintptr_t>(layers[l].kv_pool) | reinterpret_cast<uintptr_t>(layers[l].idx_pool)) & 15)
+      return MSA_ERR_INVALID_ARG;
+  }
+  if (n_blocks > 0 && (!pages || !rows)) return MSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(rows) & 15) return MSA_ERR_INVALID_ARG;
+  return launched(msa::launch_block_rows(layers, n_layers, pages, n_blocks, rows, pack,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_pack_blocks(const msa_cache* layers, int32_t n_layers, const int32_t* pages,
+                    int32_t n_blocks, uint8_t* rows, msa_stream_t stream) {
+  return block_rows(layers, n_layers, pages, n_blocks, rows, true, stream);
+}
+
+int msa_unpack_blocks(const msa_cache* layers, int32_t n_layers, const uint8_t* rows,
+                      const int32_t* pages, int32_t n_blocks, msa_stream_t stream) {
+  return block_rows(layers, n_layers, pages, n_blocks, const_cast<uint8_t*>(rows), false, stream);
 }
 
 int msa_debug_set_fault_injection(int32_t flags, uint64_t wait_limit_ns) {

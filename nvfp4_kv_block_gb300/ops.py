@@ -69,6 +69,13 @@ _SIGS = {
                                               _P, _I32, _I32, _I32, _P, _P, _P]),
     "msa_merge_splits": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P]),
     "msa_debug_set_fault_injection": (ctypes.c_int, [_I32, ctypes.c_uint64]),
+    "msa_pack_blocks": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _P]),
+    "msa_indexer_topk_range": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
+                                              _I32, _P, _P, ctypes.c_size_t, _P]),
+    "msa_indexer_merge_candidates": (ctypes.c_int, [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P,
+                                                    _P]),
+    "msa_unpack_blocks": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P]),
+    "msa_block_row_bytes": (ctypes.c_size_t, [_I32]),
     "msa_absmax": (ctypes.c_int, [_P, _I64, _P, _P]),
     "msa_encode_scale": (ctypes.c_float, [ctypes.c_float]),
     "msa_debug_fp8_page": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
@@ -196,6 +203,45 @@ def indexer_topk(cache, q_idx, w, block_table, seq_lens, q_start_loc, ws=None, s
     return sel, n_sel, ws
 
 
+def indexer_topk_range(cache, q_idx, w, block_table, seq_lens, q_start_loc, blk_lo, blk_hi, ws=None,
+                       cand=None, topk=TOPK):
+    """Local top-16 keys (uint64 stored as int64, [T, 16]) of the blocks
+    [blk_lo, blk_hi) of every sequence.  Returns (cand, ws)."""
+    T = q_idx.shape[0]
+    if tuple(q_idx.shape) != (T, IDX_HEADS, IDX_DIM) or tuple(w.shape) != (T, IDX_HEADS):
+        raise ValueError("q_idx must be [T, 8, 128] uint8 and w [T, 8] float32")
+    n_seqs, max_pages = block_table.shape
+    dev = q_idx.device
+    if ws is None:
+        ws = torch.zeros(indexer_workspace_bytes(T, max_pages), dtype=torch.uint8, device=dev)
+    if cand is None:
+        cand = torch.empty((T, topk), dtype=torch.int64, device=dev)
+    c = cache.struct()
+    _check(lib().msa_indexer_topk_range(
+        ctypes.byref(c), _ptr(q_idx, torch.uint8, "q_idx"), _ptr(w, torch.float32, "w"), IDX_HEADS,
+        _ptr(block_table, torch.int32, "block_table"), max_pages, _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(q_start_loc, torch.int32, "q_start_loc"), n_seqs, T, topk, int(blk_lo), int(blk_hi),
+        _ptr(cand, torch.int64, "cand"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()))
+    return cand, ws
+
+
+def indexer_merge_candidates(cache, cand, seq_lens, q_start_loc, max_pages, sel=None, n_sel=None,
+                             topk=TOPK):
+    """Merge [n_shards, T, 16] candidate keys into (sel [T, 17], n_sel [T])."""
+    n_shards, T, _ = cand.shape
+    dev = cand.device
+    if sel is None:
+        sel = torch.empty((T, topk + 1), dtype=torch.int32, device=dev)
+    if n_sel is None:
+        n_sel = torch.empty((T,), dtype=torch.int32, device=dev)
+    c = cache.struct()
+    _check(lib().msa_indexer_merge_candidates(
+        ctypes.byref(c), _ptr(cand, torch.int64, "cand"), n_shards, _ptr(seq_lens, torch.int32, "seq_lens"),
+        _ptr(q_start_loc, torch.int32, "q_start_loc"), seq_lens.shape[0], int(max_pages), T, topk,
+        _ptr(sel, torch.int32, "sel"), _ptr(n_sel, torch.int32, "n_sel"), _stream()))
+    return sel, n_sel
+
+
 def indexer_topk_noalloc(cache, q_idx, w, block_table, seq_lens, q_start_loc, sel=None,
                          n_sel=None, topk=TOPK):
     """indexer_topk through the allocation-free entry point (static scratch in the
@@ -253,6 +299,36 @@ def merge_splits(o_part, lse_part, out=None, lse=None):
                                   _ptr(lse_part, torch.float32, "lse_part"), T, H, S,
                                   _ptr(out, torch.float32, "out"), lse_p, _stream()))
     return out
+
+
+def block_row_bytes(n_layers):
+    return lib().msa_block_row_bytes(int(n_layers))
+
+
+def _layer_array(caches):
+    arr = (_Cache * len(caches))()
+    for i, c in enumerate(caches):
+        arr[i] = c.struct()
+    return arr
+
+
+def pack_blocks(caches, pages, rows=None):
+    """Block-outer rows [n_blocks, n_layers * 90,112] of the physical pages
+    ``pages`` (int32 [n_blocks]) from the per-layer caches."""
+    n = pages.shape[0]
+    if rows is None:
+        rows = torch.empty((n, block_row_bytes(len(caches))), dtype=torch.uint8, device=pages.device)
+    arr = _layer_array(caches)
+    _check(lib().msa_pack_blocks(arr, len(caches), _ptr(pages, torch.int32, "pages", 1), n,
+                                 _ptr(rows, torch.uint8, "rows"), _stream()))
+    return rows
+
+
+def unpack_blocks(caches, rows, pages):
+    """Write block-outer rows back into pages ``pages`` of every layer's pools."""
+    arr = _layer_array(caches)
+    _check(lib().msa_unpack_blocks(arr, len(caches), _ptr(rows, torch.uint8, "rows"),
+                                   _ptr(pages, torch.int32, "pages", 1), pages.shape[0], _stream()))
 
 
 def set_fault_injection(flags=0, wait_limit_ns=0):

@@ -23,7 +23,8 @@ float64.  The weighted sum over heads is float64.
 Parity: pinned (tests/test_oracle_indexer.py) by exact rational dot products,
 a closed-form one-hot example, a brute-force top-k over all subsets of tiny
 inputs, a full-sort cross-check, the "r <= 16 selects everything" case, the
-split-scan merge, and the hand-computed case of tests/golden/indexer_tiny.txt
+split-scan merge (range_candidates + merge_candidates over any tiling of the
+context equal select, also against brute force), and the hand-computed case of tests/golden/indexer_tiny.txt
 (19 blocks of sparse one-hot keys: block maxima at the first and the last
 token of a block, ReLU of negative dots, a tie at the cut-off, and a recent
 block whose score exceeds every other but does not compete).
@@ -68,6 +69,24 @@ def select(scores, recent, topk=16):
     order = sorted(range(recent), key=lambda b: (-scores[b], b))
     chosen = sorted(order[: min(topk, recent)])
     return chosen + [recent]
+
+
+def range_candidates(scores, recent, lo, hi, topk=16):
+    """Local top-k of one part of the context (blog, "Parallelize index work
+    across context"): blocks lo .. min(hi, recent)-1 compete by (score desc,
+    index asc); returns [(score, block)], best first."""
+    e = min(hi, recent)
+    lo = min(lo, e)
+    order = sorted(range(lo, e), key=lambda b: (-scores[b], b))
+    return [(float(scores[b]), b) for b in order[:topk]]
+
+
+def merge_candidates(parts, recent, topk=16):
+    """Top-k of the union of the parts' candidates by (score desc, index asc),
+    in ascending order, then the recent block."""
+    pool = [c for part in parts for c in part]
+    order = sorted(pool, key=lambda c: (-c[0], c[1]))
+    return sorted(b for _, b in order[:topk]) + [recent]
 
 
 def sequence_topk(q_idx, w, keys, seq_len, topk=16):

@@ -110,3 +110,40 @@ def read_index_slot(pool, page, t):
         start = t * IDX_DIM + pos * 16
         key[c * 16:(c + 1) * 16] = pool[page, start:start + 16]
     return key
+
+
+# ---- block-outer transfer rows ------------------------------------------------
+# Blog "vLLM Delivers Day-0 Support for MiniMax-M3.1-Flash", section "AMD uses
+# different conversion and communication mechanisms": a KV block spread over
+# many pages needs many reads; a block-outer layout keeps one block as one
+# contiguous row, read at once.  Reading: the row of a block holds, for every
+# layer in order, that layer's KV page (73,728 bytes) followed by its index
+# page (16,384 bytes) -- the whole decode state of the block -- so a row is
+# n_layers x 90,112 bytes; the same physical page id addresses the block in
+# every layer's pools.
+
+ROW_LAYER_BYTES = KV_PAGE_BYTES + IDX_PAGE_BYTES   # 90,112
+
+
+def pack_rows(kv_pools, idx_pools, pages):
+    """Rows [len(pages)][n_layers * 90,112] of the listed physical pages.
+
+    kv_pools, idx_pools: per layer, uint8 [n_pages, 73,728] / [n_pages, 16,384].
+    """
+    n_layers = len(kv_pools)
+    rows = np.zeros((len(pages), n_layers * ROW_LAYER_BYTES), dtype=np.uint8)
+    for i, page in enumerate(pages):
+        for layer in range(n_layers):
+            at = layer * ROW_LAYER_BYTES
+            rows[i, at:at + KV_PAGE_BYTES] = kv_pools[layer][page]
+            rows[i, at + KV_PAGE_BYTES:at + ROW_LAYER_BYTES] = idx_pools[layer][page]
+    return rows
+
+
+def unpack_rows(rows, kv_pools, idx_pools, pages):
+    """Inverse of pack_rows: write row i back into page pages[i] of every layer."""
+    for i, page in enumerate(pages):
+        for layer in range(len(kv_pools)):
+            at = layer * ROW_LAYER_BYTES
+            kv_pools[layer][page] = rows[i, at:at + KV_PAGE_BYTES]
+            idx_pools[layer][page] = rows[i, at + KV_PAGE_BYTES:at + ROW_LAYER_BYTES]

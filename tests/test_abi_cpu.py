@@ -85,6 +85,18 @@ def test_host_validation_needs_no_gpu(lib):
     assert lib.msa_merge_splits(fake, fake, 1, 2000, 2, fake, None, None) == -2
 
 
+def test_block_rows_validation_needs_no_gpu(lib):
+    P = ctypes.c_void_p
+    fake = P(16)
+    c = _cache()
+    assert lib.msa_block_row_bytes(20) == 20 * 90_112 and lib.msa_block_row_bytes(0) == 0
+    assert lib.msa_pack_blocks(ctypes.byref(c), 0, fake, 1, fake, None) == -1
+    assert lib.msa_pack_blocks(ctypes.byref(c), 129, fake, 1, fake, None) == -2
+    assert lib.msa_pack_blocks(ctypes.byref(c), 1, fake, 1, P(17), None) == -1  # unaligned rows
+    bad = _cache(head_dim=64)
+    assert lib.msa_unpack_blocks(ctypes.byref(bad), 1, fake, fake, 1, None) == -2
+
+
 def test_fault_injection_settings_are_validated_on_the_host(lib):
     assert lib.msa_debug_set_fault_injection(0x100, 0) == -1
     assert lib.msa_debug_set_fault_injection(ops.INJECT_BARRIER_TIMEOUT, 1000) == 0

@@ -188,3 +188,34 @@ def test_decode_table_equals_the_bit_field_definition():
     slow = formats.decode_e4m3(b.astype(np.int64))
     assert np.array_equal(np.isnan(fast), np.isnan(slow))
     assert np.array_equal(fast[~np.isnan(fast)], slow[~np.isnan(slow)])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_range_candidates_merge_to_the_global_selection(seed):
+    # any tiling of the competing blocks into parts: local top-16 of each part,
+    # then the merge, selects exactly what one global selection does (blog,
+    # "Parallelize index work across context"), ties included
+    rng = np.random.default_rng(100 + seed)
+    r = int(rng.integers(1, 700))
+    s = np.round(rng.uniform(0, 3, r), 1)  # many ties
+    cuts = sorted(set(int(x) for x in rng.integers(0, r + 40, int(rng.integers(0, 6)))))
+    bounds = [0] + cuts + [r + 40]
+    parts = [indexer.range_candidates(s, r, lo, hi) for lo, hi in zip(bounds[:-1], bounds[1:])]
+    assert all(len(p) <= 16 for p in parts)
+    assert indexer.merge_candidates(parts, r) == indexer.select(s, r)
+
+
+def test_range_candidates_on_tiny_inputs_equal_brute_force():
+    rng = np.random.default_rng(7)
+    for _ in range(40):
+        r = int(rng.integers(1, 9))
+        s = rng.integers(0, 3, r).astype(np.float64)
+        lo, hi = sorted(int(x) for x in rng.integers(0, r + 2, 2))
+        k = int(rng.integers(1, 5))
+        got = [b for _, b in indexer.range_candidates(s, r, lo, hi, topk=k)]
+        blocks = list(range(min(lo, min(hi, r)), min(hi, r)))
+        want = _brute_topk([s[b] for b in blocks], k) if blocks else []
+        assert sorted(got) == [blocks[i] for i in want]
+        # best first: scores non-increasing, ties by ascending block
+        pairs = [(-s[b], b) for b in got]
+        assert pairs == sorted(pairs)
