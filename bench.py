@@ -146,16 +146,19 @@ def run_gpu(args, rank, world, local_rank):
     T = wl.n_q_total
     n_splits = args.splits or ops.choose_splits(T)
     bufs = ops.DecodeBuffers(T, wl.max_pages, n_splits, dev)
+    fbufs = ops.FusedBuffers(T, wl.max_pages, dev) if args.fused else None
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
+        if fbufs is not None:
+            return ops.decode_fused(st.cache, q, qi, w, st.block_table, st.seq_lens, st.q_start_loc, fbufs)
         return ops.decode_step(st.cache, q, qi, w, st.block_table, st.seq_lens, st.q_start_loc, bufs)
 
     step()
     torch.cuda.synchronize()
-    sel = bufs.sel.cpu().numpy()
-    n_sel = bufs.n_sel.cpu().numpy()
+    sel = (fbufs or bufs).sel.cpu().numpy()
+    n_sel = (fbufs or bufs).n_sel.cpu().numpy()
     idx_bytes, kv_bytes, alg_bytes = algorithmic_bytes(wl, sel, n_sel)
 
     # the step as one CUDA graph (indexer, attention and, with several splits, the
@@ -173,6 +176,9 @@ def run_gpu(args, rank, world, local_rank):
             ops.merge_splits(bufs.o_part, bufs.lse_part, out=bufs.out)
 
     def run_step():
+        if fbufs is not None:  # the whole step in one launch
+            step()
+            return
         run_indexer()
         run_attention()
 
@@ -190,6 +196,8 @@ def run_gpu(args, rank, world, local_rank):
         with torch.cuda.graph(graph_i):
             run_indexer()
         g_step, g_idx = graph_s.replay, graph_i.replay
+    if fbufs is not None:  # one kernel: the roofline line times the step itself
+        g_idx = g_step
     for _ in range(args.warmup):
         flush.fill_(1.0)
         g_step()
@@ -243,7 +251,7 @@ def run_gpu(args, rank, world, local_rank):
                      (st.q_start_loc, h_qsl)):
             d.copy_(h, non_blocking=True)
         g_step()
-        h_out.copy_(bufs.out, non_blocking=True)
+        h_out.copy_((fbufs or bufs).out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         if i >= args.warmup:
@@ -257,7 +265,9 @@ def run_gpu(args, rank, world, local_rank):
         ms, t_idx, e2e = max_over_ranks([ms, t_idx, e2e], dev)
     return dict(wl=wl, T=T, ms=ms, t_idx=t_idx, e2e=e2e, h2d=h2d, d2h=d2h, n_splits=n_splits,
                 idx_bytes=idx_bytes, kv_bytes=kv_bytes, alg_bytes=alg_bytes, clocks=clk,
-                launches=(3 if n_splits > 1 else 2) * args.steps, insert=ins, pack=pack)
+                roof_bytes=alg_bytes if fbufs is not None else idx_bytes,
+                launches=(1 if fbufs is not None else (3 if n_splits > 1 else 2)) * args.steps, insert=ins,
+                pack=pack)
 
 
 # Algorithmic bytes of inserting one token: fp32 K and V (2 x 4 x 128 x 4), the
@@ -405,6 +415,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch kernels eagerly instead of CUDA graphs")
+    ap.add_argument("--fused", action="store_true",
+                    help="the whole step as one launch (msa_decode_fused; low concurrency, <= 64 tokens)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -445,7 +457,7 @@ def main():
     T = r["T"]
     qps = world * T / (r["ms"] * 1e-3)
     step_gbs = r["alg_bytes"] / (r["ms"] * 1e-3) / 1e9
-    idx_gbs = r["idx_bytes"] / (r["t_idx"] * 1e-3) / 1e9
+    idx_gbs = r["roof_bytes"] / (r["t_idx"] * 1e-3) / 1e9
     line = {
         "metric": "decode query tokens/s (NVFP4 sparse attention)", "value": qps, "unit": "queries/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
@@ -455,10 +467,11 @@ def main():
                 "kv_bytes": r["kv_bytes"], "achieved_gbs": step_gbs,
                 "frac_of_8tbs": step_gbs / ROOFLINE_NOMINAL_GBS,
                 f"frac_of_{peak_kind}": step_gbs / peak},
-        "roofline": {"kernel": "indexer_scan_kernel (msa_indexer_topk: block scores + selection)", "bound": "hbm",
+        "roofline": {"kernel": ("decode_fused_kernel (msa_decode_fused: the whole step)" if args.fused else
+                               "indexer_scan_kernel (msa_indexer_topk: block scores + selection)"), "bound": "hbm",
                      "achieved": idx_gbs, "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak,
                      "peak_kind": peak_kind, "traffic": committed_traffic(wl.name),
-                     "algorithmic_bytes_per_launch": r["idx_bytes"], "ms_per_launch": r["t_idx"]},
+                     "algorithmic_bytes_per_launch": r["roof_bytes"], "ms_per_launch": r["t_idx"]},
         "e2e": {"value": world * T / (r["e2e"] * 1e-3), "unit": "queries/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e"]},
         "gpu_launches": r["launches"], "n_splits": r["n_splits"], "clocks": r["clocks"],

@@ -286,6 +286,35 @@ int msa_merge_splits(const float* o_part, const float* lse_part, int32_t n_q_tot
                      msa_stream_t stream);
 
 /*
+ * The whole decode step in ONE launch, for low concurrency (blog, "AMD uses
+ * different conversion and communication mechanisms": a separate
+ * single-kernel strategy reduces launches at low concurrency; "Keep capacity,
+ * layer, and system results separate": that advantage need not hold at high
+ * concurrency, where msa_indexer_topk + msa_sparse_attn_decode +
+ * msa_merge_splits stay the faster path).  Computes exactly what those three
+ * calls compute, with the same rounding: the selection into sel / n_sel (as
+ * msa_indexer_topk) and the merged output
+ *   out fp32 [n_q_total][16][128].
+ * One cooperative launch of at most one CTA per SM runs the scan, the top-k,
+ * the attention (one page per work item, each selected block a split) and the
+ * merge, with a bounded grid barrier between phases.
+ *   ws, ws_bytes  scratch of at least msa_decode_fused_workspace_bytes(n_q_total,
+ *                 max_pages) bytes, 16-byte aligned, ZEROED before its first use
+ *                 (its first 256 bytes hold grid-barrier words that every call,
+ *                 also one that timed out, leaves at rest).  Calls sharing a
+ *                 workspace must not overlap on the GPU.
+ * Other arguments as msa_indexer_topk and msa_sparse_attn_decode.  Limits:
+ * n_seqs <= 64, n_q_total <= 64 (else MSA_ERR_UNSUPPORTED_SHAPE).
+ */
+int msa_decode_fused(const msa_cache* cache, const uint8_t* q, const uint8_t* q_idx, const float* w,
+                     int32_t n_q_heads, int32_t n_idx_heads, float softmax_scale,
+                     const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                     const int32_t* q_start_loc, int32_t n_seqs, int32_t n_q_total, int32_t topk,
+                     int32_t* sel, int32_t* n_sel, float* out, void* ws, size_t ws_bytes,
+                     msa_stream_t stream);
+size_t msa_decode_fused_workspace_bytes(int32_t n_q_total, int32_t max_pages);
+
+/*
  * Block-outer transfer rows (blog, "AMD uses different conversion and
  * communication mechanisms": a KV block kept as one contiguous row is moved in
  * one read instead of one read per page).  The row of a block holds, for every

@@ -21,6 +21,12 @@ cudaError_t launch_sparse_attn_tc(const msa_cache*, const uint8_t*, float, const
                                   float*, cudaStream_t);
 cudaError_t launch_merge(const float*, const float*, int, int, int, float*, float*, cudaStream_t);
 cudaError_t launch_debug_fp8_page(const msa_cache*, int64_t, uint8_t*, uint8_t*, cudaStream_t);
+size_t decode_fused_workspace_bytes(int, int);
+int decode_fused_max_seqs();
+int decode_fused_max_tokens();
+cudaError_t launch_decode_fused(const msa_cache*, const uint8_t*, const uint8_t*, const float*, float,
+                                const int*, int, const int*, const int*, int, int, int*, int*, float*,
+                                void*, cudaStream_t);
 cudaError_t launch_block_rows(const msa_cache*, int, const int*, int, uint8_t*, bool, cudaStream_t);
 
 namespace {
@@ -226,6 +232,37 @@ int msa_read_status(const msa_cache* cache, int32_t* host_out, msa_stream_t stre
       cudaSuccess)
     return MSA_ERR_LAUNCH_FAILED;
   return cudaStreamSynchronize(s) == cudaSuccess ? MSA_OK : MSA_ERR_LAUNCH_FAILED;
+}
+
+size_t msa_decode_fused_workspace_bytes(int32_t n_q_total, int32_t max_pages) {
+  if (n_q_total <= 0 || max_pages <= 0) return 256;
+  return msa::decode_fused_workspace_bytes(n_q_total, max_pages);
+}
+
+int msa_decode_fused(const msa_cache* cache, const uint8_t* q, const uint8_t* q_idx, const float* w,
+                     int32_t n_q_heads, int32_t n_idx_heads, float softmax_scale,
+                     const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                     const int32_t* q_start_loc, int32_t n_seqs, int32_t n_q_total, int32_t topk,
+                     int32_t* sel, int32_t* n_sel, float* out, void* ws, size_t ws_bytes,
+                     msa_stream_t stream) {
+  if (int rc = check_cache(cache)) return rc;
+  if (n_q_heads != msa::kQHeads || n_idx_heads != msa::kIdxHeads || topk != msa::kTopK)
+    return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_seqs < 0 || n_q_total < 0 || max_pages <= 0 || !(softmax_scale > 0.f) || !isfinite(softmax_scale))
+    return MSA_ERR_INVALID_ARG;
+  if (n_seqs > msa::decode_fused_max_seqs() || n_q_total > msa::decode_fused_max_tokens() ||
+      max_pages > kMaxPagesPerSeq)
+    return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_q_total > 0 && (!q || !q_idx || !w || !block_table || !seq_lens || !q_start_loc || !sel ||
+                        !n_sel || !out || !ws || n_seqs == 0))
+    return MSA_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(q_idx)) & 15) ||
+      (reinterpret_cast<uintptr_t>(ws) & 15))
+    return MSA_ERR_INVALID_ARG;
+  if (ws_bytes < msa_decode_fused_workspace_bytes(n_q_total, max_pages)) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  return launched(msa::launch_decode_fused(cache, q, q_idx, w, softmax_scale, block_table, max_pages,
+                                           seq_lens, q_start_loc, n_seqs, n_q_total, sel, n_sel, out,
+                                           ws, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t msa_block_row_bytes(int32_t n_layers) {

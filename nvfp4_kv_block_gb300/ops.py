@@ -76,6 +76,9 @@ _SIGS = {
                                                     _P]),
     "msa_unpack_blocks": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P]),
     "msa_block_row_bytes": (ctypes.c_size_t, [_I32]),
+    "msa_decode_fused": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, ctypes.c_float, _P, _I32, _P, _P, _I32,
+                                        _I32, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "msa_decode_fused_workspace_bytes": (ctypes.c_size_t, [_I32, _I32]),
     "msa_absmax": (ctypes.c_int, [_P, _I64, _P, _P]),
     "msa_encode_scale": (ctypes.c_float, [ctypes.c_float]),
     "msa_debug_fp8_page": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
@@ -379,6 +382,42 @@ class DecodeBuffers:
         # one split: its normalised output is already the answer (no merge launch)
         self.out = (self.o_part.view(n_q_total, Q_HEADS, HEAD_DIM) if n_splits == 1 else
                     torch.empty((n_q_total, Q_HEADS, HEAD_DIM), dtype=torch.float32, device=device))
+
+
+FUSED_MAX_SEQS = 64     # limits of msa_decode_fused (low concurrency)
+FUSED_MAX_TOKENS = 64
+
+
+class FusedBuffers:
+    """Outputs and scratch of the single-launch decode step (reused across steps)."""
+
+    def __init__(self, n_q_total, max_pages, device="cuda"):
+        self.T = n_q_total
+        nbytes = lib().msa_decode_fused_workspace_bytes(int(n_q_total), int(max_pages))
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)  # zeroed: barrier words
+        self.sel = torch.empty((n_q_total, TOPK + 1), dtype=torch.int32, device=device)
+        self.n_sel = torch.empty((n_q_total,), dtype=torch.int32, device=device)
+        self.out = torch.empty((n_q_total, Q_HEADS, HEAD_DIM), dtype=torch.float32, device=device)
+
+
+def decode_fused(cache, q, q_idx, w, block_table, seq_lens, q_start_loc, bufs, softmax_scale=None):
+    """The decode step in one launch (scan, top-k, attention, merge) for low
+    concurrency.  Returns bufs.out [T, 16, 128]; bufs.sel / bufs.n_sel hold the
+    selection."""
+    T = q.shape[0]
+    if tuple(q.shape) != (T, Q_HEADS, HEAD_DIM) or tuple(q_idx.shape) != (T, IDX_HEADS, IDX_DIM):
+        raise ValueError("q must be [T, 16, 128] and q_idx [T, 8, 128] uint8 (E4M3)")
+    n_seqs, max_pages = block_table.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(HEAD_DIM)
+    c = cache.struct()
+    _check(lib().msa_decode_fused(
+        ctypes.byref(c), _ptr(q, torch.uint8, "q"), _ptr(q_idx, torch.uint8, "q_idx"), _ptr(w, torch.float32, "w"),
+        Q_HEADS, IDX_HEADS, float(softmax_scale), _ptr(block_table, torch.int32, "block_table"), max_pages,
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(q_start_loc, torch.int32, "q_start_loc"), n_seqs, T, TOPK,
+        _ptr(bufs.sel, torch.int32, "sel"), _ptr(bufs.n_sel, torch.int32, "n_sel"),
+        _ptr(bufs.out, torch.float32, "out"), _ptr(bufs.ws, torch.uint8, "ws"), bufs.ws.numel(), _stream()))
+    return bufs.out
 
 
 def decode_step(cache, q, q_idx, w, block_table, seq_lens, q_start_loc, bufs, softmax_scale=None):
