@@ -20,7 +20,9 @@
 //      two swizzled tiles, S = K8 Q^T and O^T = V8^T P^T on the tensor core,
 //      softmax of the page in between; the page's normalised output and
 //      log-sum-exp are split e of the token;
-//   4. merge: CTA c combines the splits of rows (token, head) c, c + G, ...
+//   4. merge: the CTA that writes the last split of a (token, KV head) -- a
+//      counter per pair tells -- merges its splits at once (no fourth phase).
+// Short contexts prefetch the KV pages they scan into L2 for the attention.
 // Same arithmetic, rounding and layouts as the four-launch path (msa.h).
 #include "common.cuh"
 #include "topk.cuh"
@@ -47,6 +49,7 @@ constexpr int kOffSeq = kOffMisc + 64;    // s_sl [n_seqs], s_qsl [n_seqs + 1], 
 constexpr int kFSmem = kOffSeq + 4 * (3 * kFMaxSeqs + 2);
 static_assert(kOffP + 2048 <= kTopkSmem, "tiles below the persistent state");
 constexpr uint32_t kFTmemCols = 64;
+constexpr int kPrefetchPages = 96;  // contexts of at most this many scanned pages prefetch their KV
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -68,10 +71,11 @@ struct FusedParams {
   int* sel;          // [T][17]
   int* n_sel;        // [T]
   float* out;        // [T][16][128]
-  unsigned long long* sync;  // three grid-barrier words
+  unsigned long long* sync;  // two grid-barrier words
   float* scores;     // [T][max_pages][4]
   float* o_part;     // [T][17][16][128]
   float* lse_part;   // [T][17][16]
+  int* done;         // [T][4] splits written per (token, KV head)
   int* status;
   unsigned long long wait_ns;
 };
@@ -93,6 +97,59 @@ __device__ __forceinline__ bool mma4_and_wait(uint32_t d_tmem, uint64_t adesc, u
   tc_fence_after();
   // the CTA agrees: a wait that ran out in any thread ends the phase for all
   return !__syncthreads_or(!ok);
+}
+
+// A CTA has written split e of (token j, KV head g).  It counts the split in;
+// the CTA that counts the last of the token's nsel splits merges them:
+//   out = sum_e exp(lse_e - M) o_e / sum_e exp(lse_e - M),  M = max_e lse_e,
+// per query head of the group (thread = (head, two channels)), then returns
+// the counter to zero.  Ends with a barrier of the CTA.
+__device__ __forceinline__ void split_done(const FusedParams& p, int j, int g, int nsel, uint8_t* s_flag) {
+  __syncthreads();  // the CTA's split is written (CTA scope) before thread 0 counts it
+  int* flag = reinterpret_cast<int*>(s_flag);
+  if (threadIdx.x == 0) {
+    // release: this CTA's writes before the count; acquire: the other CTAs'
+    // splits, counted before, visible to the merge below
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.done + j * kKvHeads + g) : "memory");
+    *flag = old == nsel - 1;
+  }
+  __syncthreads();
+  if (*flag) {
+    const int h = threadIdx.x >> 6, ch = 2 * (threadIdx.x & 63);
+    const size_t r0 = (size_t)j * kSelStride * kQHeads + g * kGqa + h;
+    // every split's log-sum-exp and output in flight at once, then one pass
+    float l[kSelStride];
+    float2 o[kSelStride];
+#pragma unroll
+    for (int e = 0; e < kSelStride; ++e) {
+      if (e < nsel) {
+        const size_t r = r0 + (size_t)e * kQHeads;
+        l[e] = __ldcg(p.lse_part + r);
+        o[e] = __ldcg(reinterpret_cast<const float2*>(p.o_part + r * kHeadDim + ch));
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < kSelStride; ++e)
+      if (e < nsel) M = fmaxf(M, l[e]);
+    float den = 0.f, n0 = 0.f, n1 = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int e = 0; e < kSelStride; ++e) {
+        if (e < nsel) {
+          const float f = __expf(l[e] - M);
+          den += f;
+          n0 += f * o[e].x;
+          n1 += f * o[e].y;
+        }
+      }
+    }
+    float2* dst = reinterpret_cast<float2*>(p.out + ((size_t)j * kQHeads + g * kGqa + h) * kHeadDim + ch);
+    *dst = den > 0.f ? make_float2(n0 / den, n1 / den) : make_float2(0.f, 0.f);
+    if (threadIdx.x == 0) p.done[j * kKvHeads + g] = 0;
+  }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedParams p) {
@@ -142,6 +199,9 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedParams 
 
   // ---- 1. scan ----------------------------------------------------------------
   const int n_scan = s_prefix[p.n_seqs];
+  // split counters of phase 3 start at zero (two barriers order this before use)
+  for (int i = blockIdx.x * kFThreads + tid; i < p.n_q_total * kKvHeads; i += G * kFThreads) p.done[i] = 0;
+  const bool prefetch = n_scan <= kPrefetchPages;
   bool going = true;  // CTA-uniform: false once a wait ran out
   for (int x = blockIdx.x; going && x < n_scan; x += G) {
     int b = 0;
@@ -156,6 +216,20 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedParams 
         reinterpret_cast<float4*>(p.scores)[(size_t)(s.q0 + j) * p.max_pages + blk] =
             make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       continue;
+    }
+    if (prefetch && tid < kKvHeads) {
+      // short context: most of its KV pages will be selected; warm L2 with
+      // this block's (and, at the sequence's last scanned block, the recent
+      // block's) KV page while the scan runs
+      const uint8_t* kv = p.kv_pool + (size_t)phys * kKvPageBytes + tid * kHeadBytes;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kv), "r"(kHeadBytes) : "memory");
+      if (blk + 1 == s_prefix[b + 1] - s_prefix[b]) {
+        const int rp = p.block_table[(size_t)b * p.max_pages + blk + 1];
+        if (rp >= 0 && rp < p.n_pages) {
+          const uint8_t* kr = p.kv_pool + (size_t)rp * kKvPageBytes + tid * kHeadBytes;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kr), "r"(kHeadBytes) : "memory");
+        }
+      }
     }
     // the index page is stored in the swizzled operand layout: a straight copy
     const uint4* src = reinterpret_cast<const uint4*>(p.idx_pool + (size_t)phys * kIdxPageBytes);
@@ -239,11 +313,16 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedParams 
   for (int item = blockIdx.x; going && item < n_items; item += G) {
     const int j = item / (kSelStride * kKvHeads);
     const int e = (item / kKvHeads) % kSelStride, g = item % kKvHeads;
-    const int nsel = min(__ldcg(p.n_sel + j), kSelStride);
-    if (e >= nsel) continue;
     const int b = find_seq(s_qsl, p.n_seqs, j);
     const SeqInfo s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
-    if (!s.ok || j < s.q0 || j >= s.q0 + s.n_q) continue;  // flagged in the top-k
+    const bool seq_ok = s.ok && j >= s.q0 && j < s.q0 + s.n_q;  // else flagged in the top-k
+    const int nsel = seq_ok ? max(0, min(__ldcg(p.n_sel + j), kSelStride)) : 0;
+    if (e >= nsel) {
+      if (e == 0)  // nothing to attend: the token's rows are zero
+        for (int i = tid; i < kGqa * kHeadDim; i += kFThreads)
+          p.out[((size_t)j * kQHeads + g * kGqa) * kHeadDim + i] = 0.f;
+      continue;
+    }
     const int pos = s.seq_len - s.n_q + (j - s.q0), r = pos / kPageTokens;
     const int blk = __ldcg(p.sel + (size_t)j * kSelStride + e);
     int phys = -1;
@@ -260,6 +339,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedParams 
     if (phys < 0) {  // an empty split
       for (int i = tid; i < kGqa * kHeadDim; i += kFThreads) p.o_part[row0 * kHeadDim + i] = 0.f;
       if (tid < kGqa) p.lse_part[row0 + tid] = -INFINITY;
+      split_done(p, j, g, nsel, smem + kOffMisc + 16);
       continue;
     }
     const int valid = blk == r ? pos % kPageTokens + 1 : kPageTokens;
@@ -355,29 +435,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedParams 
       }
     }
     tc_fence_before();
-    __syncthreads();
-  }
-
-  // ---- 4. merge of every token's splits ----------------------------------------
-  if (tid == 0) grid_barrier(p.sync + 2, G, wc);
-  going = !__syncthreads_or(*s_abort != 0);
-  if (going && tid < kHeadDim) {
-    for (int rw = blockIdx.x; rw < p.n_q_total * kQHeads; rw += G) {
-      const int j = rw / kQHeads, h = rw % kQHeads;
-      const int nsel = max(0, min(__ldcg(p.n_sel + j), kSelStride));
-      float M = -INFINITY;
-      for (int e = 0; e < nsel; ++e) M = fmaxf(M, __ldcg(p.lse_part + ((size_t)j * kSelStride + e) * kQHeads + h));
-      float num = 0.f, den = 0.f;
-      if (M != -INFINITY) {
-        for (int e = 0; e < nsel; ++e) {
-          const size_t r = ((size_t)j * kSelStride + e) * kQHeads + h;
-          const float f = __expf(__ldcg(p.lse_part + r) - M);
-          den += f;
-          num += f * __ldcg(p.o_part + r * kHeadDim + tid);
-        }
-      }
-      p.out[(size_t)rw * kHeadDim + tid] = den > 0.f ? num / den : 0.f;
-    }
+    split_done(p, j, g, nsel, smem + kOffMisc + 16);
   }
 
   // ---- teardown ----------------------------------------------------------------
@@ -402,8 +460,9 @@ size_t decode_fused_workspace_bytes(int n_q_total, int max_pages) {
   const size_t scores = (size_t)n_q_total * max_pages * 16;
   const size_t o = (size_t)n_q_total * kSelStride * kQHeads * kHeadDim * 4;
   const size_t lse = (size_t)n_q_total * kSelStride * kQHeads * 4;
+  const size_t done = (size_t)n_q_total * kKvHeads * 4;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  return 256 + up(scores) + up(o) + up(lse);
+  return 256 + up(scores) + up(o) + up(lse) + up(done);
 }
 
 int decode_fused_max_seqs() { return kFMaxSeqs; }
@@ -426,10 +485,12 @@ cudaError_t launch_decode_fused(const msa_cache* c, const uint8_t* q, const uint
   float* o_part = reinterpret_cast<float*>(base + 256 + up((size_t)n_q_total * max_pages * 16));
   float* lse_part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(o_part) +
                                              up((size_t)n_q_total * kSelStride * kQHeads * kHeadDim * 4));
+  int* done = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(lse_part) +
+                                     up((size_t)n_q_total * kSelStride * kQHeads * 4));
   FusedParams fp{static_cast<const uint8_t*>(c->kv_pool), static_cast<const uint8_t*>(c->idx_pool), c->n_pages,
                  q, q_idx, w, block_table, max_pages, seq_lens, q_start_loc, n_seqs, n_q_total,
                  softmax_scale / c->s_enc_k * kLog2e, 1.0f / c->s_enc_v, sel, n_sel, out,
-                 static_cast<unsigned long long*>(ws), scores, o_part, lse_part, c->status,
+                 static_cast<unsigned long long*>(ws), scores, o_part, lse_part, done, c->status,
                  launch_settings().wait_ns};
   // one CTA per SM at most, as many as the largest phase has pages
   long long work = (long long)n_q_total * kSelStride * kKvHeads;

@@ -120,6 +120,44 @@ __device__ void select_token(const TopkArgs& p, int j, const int* s_sl, const in
     }
     return;
   }
+  if (n <= 64) {
+    // short rows: warp 0 alone, two keys per lane (blocks lo + lane and
+    // lo + 32 + lane), each ranked by counting over all 64 with shuffles
+    if (tid < 32) {
+      unsigned long long k0 = 0ull, k1 = 0ull;
+      if (lane < n) {
+        const float4 v = __ldcg(row + lane);
+        k0 = make_key(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)), lo + lane);
+      }
+      if (32 + lane < n) {
+        const float4 v = __ldcg(row + 32 + lane);
+        k1 = make_key(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)), lo + 32 + lane);
+      }
+      int r0 = 0, r1 = 0;
+#pragma unroll 8
+      for (int t = 0; t < 32; ++t) {
+        const unsigned long long a = __shfl_sync(0xffffffffu, k0, t), c = __shfl_sync(0xffffffffu, k1, t);
+        r0 += (a > k0) + (c > k0);
+        r1 += (a > k1) + (c > k1);
+      }
+      const bool w0 = k0 != 0ull && r0 < kTopK, w1 = k1 != 0ull && r1 < kTopK;
+      if (range_mode) {
+        if (w0) kout[r0] = k0;
+        if (w1) kout[r1] = k1;
+      } else {
+        // winners ascending: blocks grow with the lane, first the lo + lane set
+        const unsigned b0 = __ballot_sync(0xffffffffu, w0), b1 = __ballot_sync(0xffffffffu, w1);
+        const unsigned lt = (1u << lane) - 1u;
+        if (w0) out[__popc(b0 & lt)] = lo + lane;
+        if (w1) out[__popc(b0) + __popc(b1 & lt)] = lo + 32 + lane;
+        if (lane == 0) {
+          out[kTopK] = r;
+          p.n_sel[j] = kTopK + 1;
+        }
+      }
+    }
+    return;
+  }
   // Up to kRegKeys blocks per thread the keys live in registers (all loads in
   // flight at once, no shared-memory staging); longer rows are staged in
   // shared memory, or read from L2 each time beyond kTopkStage.
