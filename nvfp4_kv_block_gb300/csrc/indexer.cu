@@ -73,8 +73,9 @@ size_t scan_smem_bytes(int n_seqs) { return 1024 + kOffPrefix + 20 * (size_t)n_s
 // Relative cost of scanning one page for a sequence with n_q query tokens: a
 // fixed part per pass of up to 8 tokens (the page's bytes) plus the epilogue's
 // per-token part (a least-squares fit of per-CTA scan times on a ragged batch
-// with 1-8 tokens per sequence: a pass with 8 tokens costs about 1.4x one with 1).
-constexpr int kPassCost = 16;
+// with 1-8 tokens per sequence: 0.433 us per page and pass, 0.015 us per page
+// and query token, so a pass with 8 tokens costs about 1.25x one with 1).
+constexpr int kPassCost = 28;
 __device__ __forceinline__ long long page_weight(int n_q) {
   return (long long)((n_q + kNqMax - 1) / kNqMax) * kPassCost + n_q;
 }
@@ -240,6 +241,21 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   }
   __syncthreads();
   const long long pg_begin = s_range[0], pg_end = s_range[1];
+  if (warp == 2) {
+    // L2 prefetch of what each segment of the range starts with (index
+    // queries, head weights, the first block-table entries): after the first,
+    // a segment switch no longer waits on DRAM for them
+    int sg = 0;
+    for_each_segment(p, s_prefix, s_sl, s_qsl, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
+      if ((sg++ & 31) == lane) {
+        const uint8_t* qi = p.q_idx + (size_t)(s.q0 + j0) * kIdxHeads * kIdxDim;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qi), "r"(nq * kIdxHeads * kIdxDim) : "memory");
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.w + (size_t)(s.q0 + j0) * kIdxHeads));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.block_table + (size_t)b * p.max_pages + page0));
+      }
+      return true;
+    });
+  }
 
   if (warp == 0) {
     // ---------------- producer: index pages -----------------------------------
