@@ -48,6 +48,15 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_bf16_peak():
+    """Dense bf16 tensor TFLOP/s measured on this machine (burst: a kernel timed alone)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 def kernel_source_hash():
     """Hash of the indexer kernel's sources (its DRAM counters go stale when they change)."""
     h = hashlib.sha256()
@@ -260,6 +269,7 @@ def run_gpu(args, rank, world, local_rank):
 
     ins = time_insert(args, flush, stream, dev) if args.insert_tokens > 0 else None
     pack = time_pack(args, flush, stream, dev) if args.pack_blocks > 0 else None
+    qkvm = time_qkv(args, flush, stream, dev) if args.qkv_tokens > 0 else None
 
     if world > 1:
         ms, t_idx, e2e = max_over_ranks([ms, t_idx, e2e], dev)
@@ -267,7 +277,7 @@ def run_gpu(args, rank, world, local_rank):
                 idx_bytes=idx_bytes, kv_bytes=kv_bytes, alg_bytes=alg_bytes, clocks=clk,
                 roof_bytes=alg_bytes if fbufs is not None else idx_bytes,
                 launches=(1 if fbufs is not None else (3 if n_splits > 1 else 2)) * args.steps, insert=ins,
-                pack=pack)
+                pack=pack, qkv=qkvm)
 
 
 # Algorithmic bytes of inserting one token: fp32 K and V (2 x 4 x 128 x 4), the
@@ -275,6 +285,47 @@ def run_gpu(args, rank, world, local_rank):
 # and scales) and the FP8 index key (128 B) written.
 INSERT_READ_BYTES = 2 * 4 * 128 * 4 + 128 * 4 + 8
 INSERT_WRITE_BYTES = 576 + 128
+
+
+def time_qkv(args, flush, stream, dev):
+    """Fused QKV projection -> RMS norm -> RoPE -> FP8 queries and NVFP4 cache
+    insert of a prefill chunk (synthetic bf16 weights), as its own
+    sub-measurement; a tensor-core contraction, so its rate is FLOP/s against
+    the measured bf16 peak.  The library GEMM of the same shape alone (torch /
+    cuBLAS, no epilogue) is timed beside it for context."""
+    n, d = args.qkv_tokens, args.qkv_dmodel
+    inp = workloads.qkv_inputs(n, d, seed=11, device=dev)
+    cache = ops.KVCache(inp["n_pages"], 448.0 / 8.0, 448.0 / 6.0, dev)
+    table = ops.rope_table(inp["max_pos"], device=dev)
+    q8 = torch.empty((n, 16, 128), dtype=torch.uint8, device=dev)
+
+    def fused():
+        ops.qkv_project_insert(cache, inp["x"], inp["w"], inp["gamma_q"], inp["gamma_k"], inp["gamma_idx"], table,
+                               inp["positions"], inp["slots"], q8=q8)
+
+    def gemm():
+        torch.matmul(inp["x"], inp["w"].t())
+
+    def t(fn):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.mean(ts))
+
+    ms, ms_gemm = t(fused), t(gemm)
+    flops = 2.0 * n * d * workloads.QKV_HEADS * 128
+    return {"kernel": "qkv_fused_kernel (msa_qkv_project_insert)", "tokens": n, "d_model": d,
+            "heads_out": workloads.QKV_HEADS, "ms_per_launch": ms, "flops_per_launch": flops,
+            "achieved_tflops": flops / (ms * 1e-3) / 1e12, "library_gemm_ms": ms_gemm,
+            "library_gemm_tflops": flops / (ms_gemm * 1e-3) / 1e12}
 
 
 def time_pack(args, flush, stream, dev):
@@ -410,6 +461,9 @@ def main():
     ap.add_argument("--pack-blocks", type=int, default=2048,
                     help="blocks of the timed block-outer pack sub-measurement (0: skip)")
     ap.add_argument("--pack-layers", type=int, default=4)
+    ap.add_argument("--qkv-tokens", type=int, default=8192,
+                    help="tokens of the timed fused QKV projection + insert sub-measurement (0: skip)")
+    ap.add_argument("--qkv-dmodel", type=int, default=3072)
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -481,6 +535,13 @@ def main():
         ins["frac"] = ins["achieved_gbs"] / peak
         ins["peak_kind"] = peak_kind
         line["quantize_insert"] = ins
+    if r["qkv"] is not None:
+        qk = dict(r["qkv"])
+        tf_peak, tf_kind = measured_bf16_peak()
+        qk["peak_tflops"] = tf_peak
+        qk["frac"] = qk["achieved_tflops"] / tf_peak
+        qk["peak_kind"] = tf_kind
+        line["qkv_project_insert"] = qk
     if r["pack"] is not None:
         pk = dict(r["pack"])
         pk["frac"] = pk["achieved_gbs"] / peak

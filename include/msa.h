@@ -315,6 +315,45 @@ int msa_decode_fused(const msa_cache* cache, const uint8_t* q, const uint8_t* q_
 size_t msa_decode_fused_workspace_bytes(int32_t n_q_total, int32_t max_pages);
 
 /*
+ * Fused QKV projection -> RMS norm -> RoPE -> FP8 queries and cache insertion
+ * (blog, "Reduce both data movement and resource waits": fusing the projection
+ * with normalisation, RoPE and cache insertion avoids writing the intermediate
+ * tensor to HBM and reading it back).  The projection's accumulators stay on
+ * the SM; nothing but the outputs below is written.
+ *
+ *   x          bf16 [n_tokens][d_model] hidden states, row-major, 16-byte aligned;
+ *              d_model a multiple of 64 (64 .. 65,536).
+ *   w          bf16 [25 * 128][d_model] projection (row = output channel),
+ *              16-byte aligned: heads 0-15 queries, 16-19 keys, 20-23 values,
+ *              24 the index key (MSA_QKV_HEADS = 25 heads of 128).
+ *   gamma_q, gamma_k, gamma_idx  fp32 [128] RMS-norm gains of each head kind.
+ *   cos_sin    fp32 [max_pos][128]: cos of the 64 pair angles, then their sin
+ *              (msa_rope_table writes it); positions int32 [n_tokens] index it
+ *              (a position outside [0, max_pos) leaves the head unrotated and
+ *              sets MSA_STATUS_BAD_SEQ).
+ *   slot_mapping int64 [n_tokens] as msa_quantize_kv_insert (negative: skip).
+ *   q8         uint8 [n_tokens][16][128] out: E4M3 queries (RNE, satfinite).
+ *   y_out      fp32 [n_tokens][25][128] out, or NULL: every head's row just
+ *              before rounding (diagnostic).
+ * Per token: z = W x (fp32 accumulation of bf16 products); query, key and
+ * index-key heads y = RoPE(z / sqrt(mean(z^2) + eps) * gamma), channel pairs
+ * (i, i + 64) turned by the table's angle i: (a, b) -> (a cos - b sin,
+ * b cos + a sin); value heads y = z.  Queries -> q8; keys and values -> NVFP4
+ * in the slot, exactly the quantiser of msa_quantize_kv_insert with the
+ * cache's s_enc_k / s_enc_v; index keys -> E4M3 in the index page.
+ */
+#define MSA_QKV_HEADS 25
+int msa_qkv_project_insert(const msa_cache* cache, const void* x, const void* w, int32_t n_tokens,
+                           int32_t d_model, const float* gamma_q, const float* gamma_k,
+                           const float* gamma_idx, const float* cos_sin, int32_t max_pos,
+                           const int32_t* positions, const int64_t* slot_mapping, float eps,
+                           uint8_t* q8, float* y_out, msa_stream_t stream);
+/* RoPE table for msa_qkv_project_insert: cos_sin[pos][i] = cos(pos * base^(-2i/128))
+ * and cos_sin[pos][64 + i] = the sin, i < 64, computed in double precision and
+ * rounded to fp32 (base > 1, e.g. 10,000). */
+int msa_rope_table(float* cos_sin, int32_t max_pos, double base, msa_stream_t stream);
+
+/*
  * Block-outer transfer rows (blog, "AMD uses different conversion and
  * communication mechanisms": a KV block kept as one contiguous row is moved in
  * one read instead of one read per page).  The row of a block holds, for every

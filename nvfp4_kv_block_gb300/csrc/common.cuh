@@ -144,6 +144,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// ---- NVFP4 quantisation ------------------------------------------------------
+// E2M1 magnitude code of y / sb, round to nearest, ties to the even code,
+// saturating at 6.  Each comparison is y against midpoint * sb, which is
+// exact in fp32 (at most 7 significant bits), so the ratio is never rounded.
+__device__ __forceinline__ uint32_t e2m1_code(float y, float sb) {
+  uint32_t c = 0;
+  c += y > 0.25f * sb;   // 0   | 0.5  tie -> 0
+  c += y >= 0.75f * sb;  // 0.5 | 1    tie -> 1
+  c += y > 1.25f * sb;   // 1   | 1.5  tie -> 1
+  c += y >= 1.75f * sb;  // 1.5 | 2    tie -> 2
+  c += y > 2.5f * sb;    // 2   | 3    tie -> 2
+  c += y >= 3.5f * sb;   // 3   | 4    tie -> 4
+  c += y > 5.0f * sb;    // 4   | 6    tie -> 4
+  return sb > 0.f ? c : 0u;
+}
+
 // ---- NVFP4 -> FP8 dequantisation --------------------------------------------
 // Table entry for scale byte sb: 8 E4M3 bytes, entry m = E4M3_RNE(|e2m1(m)| * sb),
 // magnitudes m = 0..7 -> 0, 0.5, 1, 1.5, 2, 3, 4, 6.  The product has at most

@@ -27,6 +27,11 @@ int decode_fused_max_tokens();
 cudaError_t launch_decode_fused(const msa_cache*, const uint8_t*, const uint8_t*, const float*, float,
                                 const int*, int, const int*, const int*, int, int, int*, int*, float*,
                                 void*, cudaStream_t);
+int qkv_heads_out();
+cudaError_t launch_rope_table(float*, int, double, cudaStream_t);
+cudaError_t launch_qkv_fused(const msa_cache*, const void*, const void*, int, int, const float*, const float*,
+                             const float*, const float*, int, const int*, const int64_t*, float, uint8_t*,
+                             float*, cudaStream_t);
 cudaError_t launch_block_rows(const msa_cache*, int, const int*, int, uint8_t*, bool, cudaStream_t);
 
 namespace {
@@ -263,6 +268,30 @@ int msa_decode_fused(const msa_cache* cache, const uint8_t* q, const uint8_t* q_
   return launched(msa::launch_decode_fused(cache, q, q_idx, w, softmax_scale, block_table, max_pages,
                                            seq_lens, q_start_loc, n_seqs, n_q_total, sel, n_sel, out,
                                            ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_rope_table(float* cos_sin, int32_t max_pos, double base, msa_stream_t stream) {
+  if (max_pos < 0 || (max_pos > 0 && !cos_sin) || !(base > 1.0) || !isfinite(base)) return MSA_ERR_INVALID_ARG;
+  return launched(msa::launch_rope_table(cos_sin, max_pos, base, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int msa_qkv_project_insert(const msa_cache* cache, const void* x, const void* w, int32_t n_tokens,
+                           int32_t d_model, const float* gamma_q, const float* gamma_k,
+                           const float* gamma_idx, const float* cos_sin, int32_t max_pos,
+                           const int32_t* positions, const int64_t* slot_mapping, float eps,
+                           uint8_t* q8, float* y_out, msa_stream_t stream) {
+  if (int rc = check_cache(cache)) return rc;
+  if (n_tokens < 0 || max_pos <= 0 || !(eps >= 0.f) || !isfinite(eps)) return MSA_ERR_INVALID_ARG;
+  if (d_model < 64 || d_model % 64 != 0 || d_model > 65536) return MSA_ERR_UNSUPPORTED_SHAPE;
+  if (n_tokens > 0 && (!x || !w || !gamma_q || !gamma_k || !gamma_idx || !cos_sin || !positions ||
+                       !slot_mapping || !q8))
+    return MSA_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(cos_sin) |
+        reinterpret_cast<uintptr_t>(q8) | reinterpret_cast<uintptr_t>(y_out)) & 15))
+    return MSA_ERR_INVALID_ARG;
+  return launched(msa::launch_qkv_fused(cache, x, w, n_tokens, d_model, gamma_q, gamma_k, gamma_idx, cos_sin,
+                                        max_pos, positions, slot_mapping, eps, q8, y_out,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t msa_block_row_bytes(int32_t n_layers) {

@@ -15,21 +15,6 @@
 namespace msa {
 namespace {
 
-// E2M1 magnitude code of y / sb, round to nearest, ties to the even code,
-// saturating at 6.  Each comparison is y against midpoint * sb, which is
-// exact in fp32 (at most 7 significant bits), so the ratio is never rounded.
-__device__ __forceinline__ uint32_t e2m1_code(float y, float sb) {
-  uint32_t c = 0;
-  c += y > 0.25f * sb;   // 0   | 0.5  tie -> 0
-  c += y >= 0.75f * sb;  // 0.5 | 1    tie -> 1
-  c += y > 1.25f * sb;   // 1   | 1.5  tie -> 1
-  c += y >= 1.75f * sb;  // 1.5 | 2    tie -> 2
-  c += y > 2.5f * sb;    // 2   | 3    tie -> 2
-  c += y >= 3.5f * sb;   // 3   | 4    tie -> 4
-  c += y > 5.0f * sb;    // 4   | 6    tie -> 4
-  return sb > 0.f ? c : 0u;
-}
-
 __global__ void __launch_bounds__(256) quantize_insert_kernel(
     uint8_t* __restrict__ kv_pool, uint8_t* __restrict__ idx_pool, int64_t n_pages,
     const float* __restrict__ k, const float* __restrict__ v, const float* __restrict__ idx_k,

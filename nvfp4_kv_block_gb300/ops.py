@@ -79,6 +79,9 @@ _SIGS = {
     "msa_decode_fused": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, ctypes.c_float, _P, _I32, _P, _P, _I32,
                                         _I32, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "msa_decode_fused_workspace_bytes": (ctypes.c_size_t, [_I32, _I32]),
+    "msa_qkv_project_insert": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P,
+                                              ctypes.c_float, _P, _P, _P]),
+    "msa_rope_table": (ctypes.c_int, [_P, _I32, ctypes.c_double, _P]),
     "msa_absmax": (ctypes.c_int, [_P, _I64, _P, _P]),
     "msa_encode_scale": (ctypes.c_float, [ctypes.c_float]),
     "msa_debug_fp8_page": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
@@ -332,6 +335,37 @@ def unpack_blocks(caches, rows, pages):
     arr = _layer_array(caches)
     _check(lib().msa_unpack_blocks(arr, len(caches), _ptr(rows, torch.uint8, "rows"),
                                    _ptr(pages, torch.int32, "pages", 1), pages.shape[0], _stream()))
+
+
+QKV_HEADS = 25  # MSA_QKV_HEADS
+
+
+def rope_table(max_pos, base=10000.0, device="cuda"):
+    """fp32 [max_pos, 128] RoPE cos / sin table (msa_rope_table)."""
+    t = torch.empty((max_pos, 128), dtype=torch.float32, device=device)
+    _check(lib().msa_rope_table(_ptr(t, torch.float32, "cos_sin"), int(max_pos), float(base), _stream()))
+    return t
+
+
+def qkv_project_insert(cache, x, w, gamma_q, gamma_k, gamma_idx, cos_sin, positions, slot_mapping,
+                       eps=1e-6, q8=None, y_out=None):
+    """Fused projection -> RMS norm -> RoPE -> FP8 queries (returned, [n, 16, 128])
+    and NVFP4 / FP8 cache insertion.  ``y_out`` ([n, 25, 128] fp32) receives the
+    rows before rounding when given."""
+    n, d = x.shape
+    if tuple(w.shape) != (QKV_HEADS * HEAD_DIM, d):
+        raise ValueError("w must be [25 * 128, d_model] bf16")
+    if q8 is None:
+        q8 = torch.empty((n, Q_HEADS, HEAD_DIM), dtype=torch.uint8, device=x.device)
+    yp = ctypes.c_void_p(None) if y_out is None else _ptr(y_out, torch.float32, "y_out")
+    c = cache.struct()
+    _check(lib().msa_qkv_project_insert(
+        ctypes.byref(c), _ptr(x, torch.bfloat16, "x", 2), _ptr(w, torch.bfloat16, "w", 2), n, d,
+        _ptr(gamma_q, torch.float32, "gamma_q"), _ptr(gamma_k, torch.float32, "gamma_k"),
+        _ptr(gamma_idx, torch.float32, "gamma_idx"), _ptr(cos_sin, torch.float32, "cos_sin", 2),
+        cos_sin.shape[0], _ptr(positions, torch.int32, "positions"), _ptr(slot_mapping, torch.int64, "slot_mapping"),
+        float(eps), _ptr(q8, torch.uint8, "q8"), yp, _stream()))
+    return q8
 
 
 def set_fault_injection(flags=0, wait_limit_ns=0):

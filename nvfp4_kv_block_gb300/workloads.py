@@ -186,3 +186,25 @@ def config(i):
 def custom(name, seq_lens, n_q, seed, outliers=False, permuted=False):
     return Workload(name, tuple(int(x) for x in seq_lens), tuple(int(x) for x in n_q), seed,
                     outliers, permuted)
+
+
+# -- fused projection inputs (synthetic weights: no trained checkpoint) -----------
+QKV_HEADS = 25  # 16 query, 4 key, 4 value, 1 index-key heads of 128
+
+
+def qkv_inputs(n_tokens, d_model, seed, device, max_pos=65536, n_pages=None):
+    """Seeded inputs of the fused QKV projection: bf16 hidden states x [n, d]
+    ~ N(0, 1), bf16 weights w [25 * 128, d] ~ N(0, 1/d), fp32 RMS-norm gains
+    ~ 1 + 0.1 N(0, 1) (query, key, index key), int32 positions uniform in
+    [0, max_pos), and int64 slots: distinct random slots of a pool of n_pages
+    pages (default: just enough pages)."""
+    g = _gen(device, seed, _META, 17)
+    x = torch.randn((n_tokens, d_model), generator=g, device=device).to(torch.bfloat16)
+    w = (torch.randn((QKV_HEADS * HEAD_DIM, d_model), generator=g, device=device) / math.sqrt(d_model)).to(torch.bfloat16)
+    gammas = [1.0 + 0.1 * torch.randn(HEAD_DIM, generator=g, device=device) for _ in range(3)]
+    positions = torch.randint(0, max_pos, (n_tokens,), generator=g, device=device, dtype=torch.int32)
+    if n_pages is None:
+        n_pages = max(1, math.ceil(n_tokens / PAGE_TOKENS) + 1)
+    slots = torch.randperm(n_pages * PAGE_TOKENS, generator=g, device=device)[:n_tokens].to(torch.int64)
+    return dict(x=x, w=w, gamma_q=gammas[0], gamma_k=gammas[1], gamma_idx=gammas[2], positions=positions,
+                slots=slots, n_pages=n_pages, max_pos=max_pos)

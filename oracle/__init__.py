@@ -26,4 +26,4 @@ the header of the module that implements it.
 Parity status per function is stated in each module header.
 """
 
-from . import formats, nvfp4, layout, indexer, attention, decode  # noqa: F401
+from . import formats, nvfp4, layout, indexer, attention, decode, qkv  # noqa: F401
