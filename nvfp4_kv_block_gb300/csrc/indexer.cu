@@ -8,19 +8,20 @@
 // once, by one CTA, and the selection runs over all of them).
 //
 // Scan (hot loop), one persistent CTA per SM.  The pages to scan (blocks
-// 0..r_last-1 of every sequence) are flattened and cut into equal contiguous
-// ranges, one per CTA.  Warp-specialised pipeline:
-//   warp 0      TMA producer: one 16 KB cp.async.bulk per index page into an
-//               8-stage shared-memory ring (128 KB in flight per SM); also writes
-//               the index-query tile (B operand) of each sequence segment;
-//   warp 1      MMA issuer: per page, 4 x tcgen05.mma kind::f8f6f4 with M = 128
-//               tokens (the page, A from shared memory), N = 8 heads x query
-//               tokens (B), K = 128 dims, fp32 accumulators in tensor memory,
-//               double-buffered; tcgen05.commit frees the stage and hands the
-//               accumulator to the epilogue;
-//   warps 2-5   epilogue: tcgen05.ld of one token row per thread, ReLU, head
-//               weights, sum over heads, block max over the 128 rows; one fp32
-//               per (query token, block) is written.
+// 0..r_last-1 of every sequence) are flattened and cut into contiguous ranges
+// of equal weighted cost, one per CTA.  Warp-specialised pipeline:
+//   warp 0      TMA producer: one 16 KB cp.async.bulk per index page into a
+//               6-stage shared-memory ring;
+//   warps 1-2   MMA issuers, alternate pages: per page, 4 x tcgen05.mma
+//               kind::f8f6f4 with M = 128 tokens (the page, A from shared
+//               memory), N = 8 heads x query tokens (B: the segment's index
+//               queries, one copy per issuer), K = 128 dims, fp32 accumulators
+//               in tensor memory (6 buffers); tcgen05.commit frees the stage and
+//               hands the accumulator to the epilogue;
+//   warps 3-14  epilogue, three sets of four taking every third page:
+//               tcgen05.ld of one token row per thread, ReLU, head weights, sum
+//               over heads, block max over the 128 rows; one fp32 per (query
+//               token, block) and quarter is written.
 // The index page is stored pre-swizzled (chunk c of token t at chunk c ^ (t&7)),
 // which is exactly the 128-byte-swizzled K-major operand layout, so a plain
 // bulk copy lands it ready for the tensor core.
@@ -52,17 +53,19 @@ struct ScanParams {
   unsigned long long* cand;    // range mode: [T][16] local top-16 keys instead of sel / n_sel
 };
 
-constexpr int kScanThreads = 320;  // 10 warps
-constexpr int kStages = 8;
+constexpr int kScanThreads = 480;  // 15 warps: producer, 2 MMA issuers, 3 epilogue sets of 4
+constexpr int kStages = 6;
 constexpr int kNqMax = 8;                       // query tokens per pass
 constexpr int kBRows = kNqMax * kIdxHeads;      // 64
 constexpr int kBBytes = kBRows * kIdxDim;       // 8 KB
-constexpr int kAccs = 4;                        // accumulators in tensor memory
-constexpr int kTmemCols = kAccs * 64;           // 256 columns
+constexpr int kMmaWarps = 2;                    // MMA issuers, pages it with it % 2 == issuer
+constexpr int kEpiSets = 3;                     // epilogue sets, pages it with it % 3 == set
+constexpr int kAccs = kMmaWarps * kEpiSets;     // 6 accumulators: acc = it % 6 fixes both
+constexpr int kTmemCols = 512;                  // 6 x 64 columns, allocated as a power of two
 constexpr int kOffStages = 0;
 constexpr int kOffB = kStages * kIdxPageBytes;  // 131,072
-constexpr int kOffBars = kOffB + 2 * kBBytes;   // 147,456
-constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccs + 1;
+constexpr int kOffBars = kOffB + 2 * kMmaWarps * kBBytes;  // two B slots per MMA issuer
+constexpr int kNumBars = 2 * kStages + 2 * kMmaWarps + 2 * kAccs + kMmaWarps;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffPrefix = kOffMisc + 32;  // misc: tmem slot, abort, page range [2] (int64), copies issued
 
@@ -72,10 +75,10 @@ size_t scan_smem_bytes(int n_seqs) { return 1024 + kOffPrefix + 20 * (size_t)n_s
 
 // Relative cost of scanning one page for a sequence with n_q query tokens: a
 // fixed part per pass of up to 8 tokens (the page's bytes) plus the epilogue's
-// per-token part (a least-squares fit of per-CTA scan times on a ragged batch
-// with 1-8 tokens per sequence: 0.433 us per page and pass, 0.015 us per page
-// and query token, so a pass with 8 tokens costs about 1.25x one with 1).
-constexpr int kPassCost = 28;
+// per-token part.  With two MMA issuers and three epilogue sets the scan of the
+// ragged batch streams its pages at the DRAM's pace, so the per-token part is
+// small: 28, 48 and 96 for the fixed part measured within 1.5% of each other.
+constexpr int kPassCost = 64;
 __device__ __forceinline__ long long page_weight(int n_q) {
   return (long long)((n_q + kNqMax - 1) / kNqMax) * kPassCost + n_q;
 }
@@ -127,11 +130,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   // barrier addresses
   auto full = [&](int i) { return bar0 + 8 * i; };
   auto empty = [&](int i) { return bar0 + 8 * (kStages + i); };
-  auto bfull = [&](int i) { return bar0 + 8 * (2 * kStages + i); };
-  auto bempty = [&](int i) { return bar0 + 8 * (2 * kStages + 2 + i); };
-  auto tfull = [&](int i) { return bar0 + 8 * (2 * kStages + 4 + i); };
-  auto tempty = [&](int i) { return bar0 + 8 * (2 * kStages + 4 + kAccs + i); };
-  const uint32_t done_bar = bar0 + 8 * (2 * kStages + 4 + 2 * kAccs);
+  auto bempty = [&](int i) { return bar0 + 8 * (2 * kStages + i); };  // B slot i = 2 issuer + slot
+  auto tfull = [&](int i) { return bar0 + 8 * (2 * kStages + 2 * kMmaWarps + i); };
+  auto tempty = [&](int i) { return bar0 + 8 * (2 * kStages + 2 * kMmaWarps + kAccs + i); };
+  auto done_bar = [&](int m) { return bar0 + 8 * (2 * kStages + 2 * kMmaWarps + 2 * kAccs + m); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   const WaitCtl wc{s_abort, p.wait_ns};
@@ -154,15 +156,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
       mbar_init(full(i), 1);
       mbar_init(empty(i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bfull(i), 1);
-      mbar_init(bempty(i), 1);
-    }
+    for (int i = 0; i < 2 * kMmaWarps; ++i) mbar_init(bempty(i), 1);
     for (int i = 0; i < kAccs; ++i) {
       mbar_init(tfull(i), 1);
       mbar_init(tempty(i), 4);
     }
-    mbar_init(done_bar, 1);
+    for (int m = 0; m < kMmaWarps; ++m) mbar_init(done_bar(m), 1);
     *s_abort = 0;
     *s_issued = 0;
     fence_barrier_init();
@@ -241,7 +240,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   }
   __syncthreads();
   const long long pg_begin = s_range[0], pg_end = s_range[1];
-  if (warp == 2) {
+  if (warp == 1 + kMmaWarps) {
     // L2 prefetch of what each segment of the range starts with (index
     // queries, head weights, the first block-table entries): after the first,
     // a segment switch no longer waits on DRAM for them
@@ -286,11 +285,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
       return true;
     });
     if (lane == 0) *s_issued = it;  // copies issued, for the drain after an abort
-  } else if (warp == 1) {
-    // ---------------- MMA warp: B tile of each segment, then the MMAs ----------
+  } else if (warp <= kMmaWarps) {
+    // ---------------- MMA warps: B tile of each segment, then the MMAs ----------
+    // issuer m takes the pages with it % 2 == m: one thread issues a
+    // tcgen05.mma every ~140 cycles, four per page, so two issuers keep up
+    // with the page stream; each builds its own copy of the segment's B tile
+    const int mw = warp - 1;
     int it = 0, sg = 0;
     for_each_segment(p, s_prefix, s_sl, s_qsl, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
-      const int slot = sg & 1;
+      const int slot = 2 * mw + (sg & 1);
       // the MMAs that read this slot two segments ago must be done
       if (!mbar_wait(bempty(slot), ((sg >> 1) & 1) ^ 1, wc)) return false;
       // index queries of tokens j0..j0+nq-1 -> rows (token, head), 128-byte
@@ -320,6 +323,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
         const uint32_t idesc = umma_idesc_e4m3(128, n_rows);
         const uint64_t bdesc = umma_desc_sw128(sbase + kOffB + slot * kBBytes);
         for (int page = page0; page < page1; ++page, ++it) {
+          if ((it & 1) != mw) continue;
           const int st = it % kStages, acc = it % kAccs;
           if (!mbar_wait(full(st), (it / kStages) & 1, wc)) { ok = false; break; }
           if (!mbar_wait(tempty(acc), ((it / kAccs) & 1) ^ 1, wc)) { ok = false; break; }
@@ -339,18 +343,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
       return ok;
     });
   } else {
-    // ---------------- epilogue: two sets of four warps, set = page parity ------
-    // warps 2..5 and 6..9 -> TMEM lane quadrants 2,3,0,1; each warp writes the
-    // max over its 32 token rows, the top-k phase takes the max of the four.
-    const int quad = warp & 3, set = (warp - 2) >> 2;
+    // ---------------- epilogue: three sets of four warps, set = it % 3 ----------
+    // warps 3..6, 7..10, 11..14 -> TMEM lane quadrants 3,0,1,2; each warp
+    // writes the max over its 32 token rows, the top-k phase takes the max of
+    // the four.
+    const int quad = warp & 3, set = (warp - 1 - kMmaWarps) >> 2;
     int it = 0;
     for_each_segment(p, s_prefix, s_sl, s_qsl, pg_begin, pg_end, [&](int b, const SeqInfo& s, int j0, int nq, int page0, int page1) {
-      float wr[kNqMax][kIdxHeads];
-#pragma unroll
-      for (int jj = 0; jj < kNqMax; ++jj)
-#pragma unroll
-        for (int h = 0; h < kIdxHeads; ++h)
-          wr[jj][h] = jj < nq ? p.w[(size_t)(s.q0 + j0 + jj) * kIdxHeads + h] : 0.f;
+      // head weights of the segment's tokens: read per page (L1 hits after the
+      // first), not held in registers
+      const float4* wseg = reinterpret_cast<const float4*>(p.w + (size_t)(s.q0 + j0) * kIdxHeads);
       const int* bt = p.block_table + (size_t)b * p.max_pages;
       float* srow = p.scores + ((size_t)(s.q0 + j0 + lane) * p.max_pages) * 4 + quad;
       int bt_nxt = page0 + lane < page1 ? bt[page0 + lane] : 0;
@@ -361,18 +363,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
           bt_nxt = page + 32 + lane < page1 ? bt[page + 32 + lane] : 0;
         }
         const int phys = __shfl_sync(0xffffffffu, bt_cur, (page - page0) & 31);
-        if ((it & 1) != set) continue;
+        if (it % kEpiSets != set) continue;
         const int acc = it % kAccs;
         if (!mbar_wait(tfull(acc), (it / kAccs) & 1, wc)) return false;
         tc_fence_after();
-        // every column the page needs (16 per pair of query tokens: 2 x 8
-        // heads) in one load, then one wait, so the tensor-memory latency is
-        // paid once per page; the accumulator is released before the math
+        // the columns of up to four query tokens (8 heads each) per load, the
+        // loads of a page back to back, one wait per half; the accumulator is
+        // released before the second half's math
         const uint32_t ta = tmem + ((uint32_t)(32 * quad) << 16) + acc * 64;
-        uint32_t v[64];
-        if (nq <= 2) tmem_ld32x32b_x16(ta, v);
-        else if (nq <= 4) tmem_ld32x32b_x32(ta, v);
-        else tmem_ld32x32b_x64(ta, v);
+        uint32_t v0[32], v1[32];
+        if (nq <= 2) tmem_ld32x32b_x16(ta, v0);
+        else tmem_ld32x32b_x32(ta, v0);
+        if (nq > 4) tmem_ld32x32b_x32(ta + 32, v1);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -381,9 +383,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
 #pragma unroll
         for (int jj = 0; jj < kNqMax; ++jj) {
           if (jj < nq) {
+            const float4 wa = __ldg(wseg + 2 * jj), wb = __ldg(wseg + 2 * jj + 1);
+            const float wh[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
             float sc = 0.f;
 #pragma unroll
-            for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[jj][h], fmaxf(__uint_as_float(v[8 * jj + h]), 0.f), sc);
+            for (int h = 0; h < kIdxHeads; ++h)
+              sc = fmaf(wh[h], fmaxf(__uint_as_float(jj < 4 ? v0[8 * jj + h] : v1[8 * (jj - 4) + h]), 0.f), sc);
             const float x = warp_max_f32(sc);
             if (lane == jj) mine = x;
           }
@@ -405,9 +410,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
     // after an abort (bounded waits that ignore the flag): no tcgen05.mma may
     // still run when tensor memory is released, and no bulk copy may still be
     // writing the ring when its shared memory is reused or the CTA exits
-    if (warp == 1 && lane == 0) {
-      umma_commit(done_bar);
-      mbar_wait_drain(done_bar, 0, p.wait_ns);
+    if (warp >= 1 && warp <= kMmaWarps && lane == 0) {
+      umma_commit(done_bar(warp - 1));
+      mbar_wait_drain(done_bar(warp - 1), 0, p.wait_ns);
     }
     if (warp == 0 && lane == 0) {
       const int n = *s_issued;
