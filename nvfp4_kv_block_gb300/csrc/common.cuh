@@ -247,6 +247,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 1; i < kSpinLimit; ++i) {
+    __nanosleep(32);  // a short back-off: waiting warps leave issue slots to the others
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 15) == 0 && (*w.abort || globaltimer_ns() - t0 > w.limit_ns)) break;
   }
