@@ -17,85 +17,76 @@
 //                q_start_loc), the selected blocks, their physical pages and the
 //                tokens visible in each, and the 4 query rows as a swizzled
 //                tile, into a 4-deep ring of item records;
-//   warp 1       TMA producer: per page two 9 KB cp.async.bulk copies, the K
-//                half (codes + scales) and the V half, into two 6-stage rings;
+//   warp 1       TMA producer: one 18,432-byte cp.async.bulk copy per page (the
+//                KV head's K and V codes and scales) into a ring of stages;
 //   warp 2       QK issuer: S = K8 Q^T (kind::f8f6f4, M = 128 tokens, N = 16: the
 //                4 query heads, zero padded, K = 128, A from tensor memory);
-//   warp 3       PV issuer: O^T = V8^T P (A = the V tile read MN-major, no
-//                transpose, B = P), one of 4 TMEM O buffers per page; its one
-//                commit per page completes the page's O barrier, which also
+//   warp 3       PV issuer: O^T += V8^T P (A = the V tile read MN-major, no
+//                transpose, B = P), accumulated in tensor memory over the
+//                item's pages (one buffer per item parity); its commit per page
 //                frees the page's V tile and P tile;
-//   warps 4 ..   softmax, kSets sets of 4 warps; set s takes the pages with
-//                e % kSets == s and keeps its own running (m, l, o): thread = token
-//                row of S: page max per head, P = exp2 relative to the page max,
-//                scaled by 2^8 and split into two E4M3 terms (value + rounding
-//                remainder) as the B operand of PV; thread = channel: the page's
-//                O folded into the running state.  At the item's end sets
-//                1 .. kSets - 1 hand their states to set 0, which merges them and
-//                writes the normalised partial (O, LSE).  The LSE merge kernel
-//                combines the splits;
-//   next 4 x kConvSets warps: K conversion, thread = (token, part of the row):
-//                NVFP4 -> FP8 through a 256-entry shared table of scaled E4M3
-//                values and byte permutes, written with tcgen05.st straight into
-//                tensor memory (the A operand);
-//   last 4 x kConvSets warps: V conversion, the same into a 128-byte-swizzled
-//                shared-memory tile (3 tiles).
+//   warps 4-7    softmax, thread = token row of S: P = 256 * 2^(x - m) for a
+//                reference m per head that changes only when a row of the page
+//                exceeds it by more than kGrowth (then m = page max + kHeadroom,
+//                the running row sums and the O accumulator are rescaled);
+//                P is written as two E4M3 terms (value + rounding remainder),
+//                the B operand of PV.  At the item's end, thread = channel: the
+//                normalised partial (O, LSE); the LSE merge kernel combines
+//                the splits;
+//   warps 8 ..   kGroups conversion warpgroups; group g converts the pages with
+//                e % kGroups == g, thread = token: NVFP4 -> FP8 through a
+//                256-entry shared table of scaled E4M3 values and byte
+//                permutes, K written with tcgen05.st straight into tensor memory
+//                (the A operand of QK), V into a 128-byte-swizzled shared tile.
 #include "common.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kConvSets = 2;   // warps per token row of K (and of V): each converts 4 / kConvSets chunks
-constexpr int kSets = 2;       // softmax sets of 4 warps; set s takes the pages with e % kSets == s
-constexpr int kWarpConv0 = 4 + 4 * kSets;  // first conversion warp
-constexpr int kThreads = 32 * (kWarpConv0 + 8 * kConvSets);
-constexpr int kStages = 6;     // raw K and raw V ring depth
+constexpr int kGroups = 2;     // conversion warpgroups
+constexpr int kWarpConv0 = 8;  // warps 0-3 roles, 4-7 softmax
+constexpr int kThreads = 32 * (kWarpConv0 + 4 * kGroups);
+constexpr int kStages = 6;     // raw page ring
 constexpr int kRecs = 4;       // item records in flight
-constexpr int kK8Slots = 4;    // K8 buffers in tensor memory (a power of two: slot = e & 3)
-constexpr int kV8Tiles = 4;    // V8 tiles in shared memory (a power of two)
-constexpr int kPO = 4;         // P tiles and O buffers
-// a V tile is reused only after the PV of page e - kV8Tiles completes the O
-// barrier of that page; with kV8Tiles <= kPO no later phase of that barrier can
-// complete before the V warps have seen it (that would need page e's V tile)
-static_assert(kV8Tiles <= kPO, "V tile reuse waits on the O barrier of page e - kV8Tiles");
-static_assert(kV8Tiles == kPO, "a V tile and the O buffer of its page share the slot index");
-constexpr int kHalfBytes = kHeadBytes / 2;  // 9,216: codes + scales of K (or V)
-constexpr int kTileBytes = 16384;           // [128 rows][128 B], swizzled
-constexpr int kOffV8 = 0;                                   // kV8Tiles V8 tiles
-constexpr int kOffQ = kV8Tiles * kTileBytes;                // kRecs x [16 rows][128 B]
-constexpr int kOffP = kOffQ + kRecs * 2048;                 // kPO x [128 tokens][16 B]
-constexpr int kOffKRaw = kOffP + kPO * 2048;                // kStages x 9,216
-constexpr int kOffVRaw = kOffKRaw + kStages * kHalfBytes;   // kStages x 9,216
-constexpr int kOffTab = kOffVRaw + kStages * kHalfBytes;    // uint2 [256]
-constexpr int kOffRec = kOffTab + 2048;                     // kRecs x 256 B
-constexpr int kOffMerge = kOffRec + kRecs * 256;            // [kSets - 1][2] x (o [4][128], m [4], L [4]) floats
-constexpr int kMergeBytes = (4 * 128 + 8) * 4;
-constexpr int kMergeBufs = 2 * (kSets - 1);                 // per helper set, per item parity
-constexpr int kOffBars = kOffMerge + kMergeBufs * kMergeBytes;
+constexpr int kSlots = 4;      // K8 buffers (tensor memory), V8 tiles and P tiles: slot = e % kSlots
+// A group waits only for its own pages' slots and stages; for a parity wait
+// never to see a phase two behind, the same group must own every page of a
+// slot (and of a stage): kGroups divides both ring sizes.
+static_assert(kSlots % kGroups == 0 && kStages % kGroups == 0, "groups own whole slots and stages");
+constexpr int kTileBytes = 16384;                      // [128 rows][128 B], swizzled
+constexpr int kOffV8 = 0;                              // kSlots V8 tiles
+constexpr int kOffQ = kSlots * kTileBytes;             // kRecs x [16 rows][128 B]
+constexpr int kOffP = kOffQ + kRecs * 2048;            // kSlots x [128 tokens][16 B]
+constexpr int kOffRaw = kOffP + kSlots * 2048;         // kStages x 18,432
+constexpr int kOffTab = kOffRaw + kStages * kHeadBytes;  // uint2 [256]
+constexpr int kOffRec = kOffTab + 2048;                // kRecs x 256 B
+constexpr int kOffRed = kOffRec + kRecs * 256;         // float [4 warps][4 heads] page maxima
+constexpr int kOffRedL = kOffRed + 64;                 // float [4 warps][4 heads] row sums
+constexpr int kOffBars = kOffRedL + 64;
 // barrier indices
-constexpr int kKrFull = 0, kKrEmpty = kStages, kVrFull = 2 * kStages, kVrEmpty = 3 * kStages;
-constexpr int kK8Full = 4 * kStages, kK8Empty = kK8Full + kK8Slots, kSFull = kK8Empty + kK8Slots,
-              kSEmpty = kSFull + kSets, kV8Full = kSEmpty + kSets, kPFull = kV8Full + kV8Tiles,
-              kOFull = kPFull + kPO,
-              kOEmpty = kOFull + kPO, kRecFull = kOEmpty + kPO, kRecEmpty = kRecFull + kRecs,
-              kMergeFull = kRecEmpty + kRecs, kMergeEmpty = kMergeFull + kMergeBufs,
-              kDone = kMergeEmpty + kMergeBufs,
+constexpr int kRawFull = 0, kRawEmpty = kStages, kK8Full = 2 * kStages, kK8Empty = kK8Full + kSlots,
+              kSFull = kK8Empty + kSlots, kSEmpty = kSFull + 2, kV8Full = kSEmpty + 2,
+              kPFull = kV8Full + kSlots, kPVDone = kPFull + kSlots, kOFree = kPVDone + kSlots,
+              kRecFull = kOFree + 2, kRecEmpty = kRecFull + kRecs, kDone = kRecEmpty + kRecs,
               kNumBars = kDone + 2;  // kDone: QK issuer, kDone + 1: PV issuer
-constexpr int kOffMisc = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;  // tmem, abort, issued K/V
-constexpr int kOffRed = kOffMisc + 16;        // float [kSets][2][4 warps][4 heads] page maxima
-constexpr int kOffRedL = kOffRed + 128 * kSets;  // float [kSets][4 warps][4 heads] row sums
-constexpr int kOffQsl = kOffRedL + 64 * kSets;   // int [n_seqs + 1] copy of q_start_loc
-constexpr uint32_t kTmS = 32 * kK8Slots;      // TMEM columns: K8 slot i at 32 i, S slot s at kTmS + 16 s,
-constexpr uint32_t kTmO = kTmS + 16 * kSets;  // O buffers at kTmO + 16 i
+constexpr int kOffMisc = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;  // tmem, abort, issued pages
+constexpr int kOffQsl = kOffMisc + 16;  // int [n_seqs + 1] copy of q_start_loc
+constexpr uint32_t kTmS = 32 * kSlots;  // TMEM columns: K8 slot i at 32 i, S slot s at kTmS + 16 s,
+constexpr uint32_t kTmO = kTmS + 32;    // O buffer b at kTmO + 16 b
 constexpr uint32_t kTmemCols = 256;
-static_assert(kTmO + 16 * kPO <= kTmemCols, "tensor memory columns");
-constexpr int kRecEmptyCount = 1 + 8 * kConvSets + 1 + 1 + 4 * kSets;  // producer, K and V, QK, PV, softmax
-static_assert(kPO > kSets, "a set writes P of page e before it folds page e - kSets");
+static_assert(kTmO + 32 <= kTmemCols, "tensor memory columns");
+// producer, QK issuer (a commit), PV issuer, 4 softmax warps, the conversion warps
+constexpr int kRecEmptyCount = 3 + 4 + 4 * kGroups;
+// P = 256 * 2^(x - m) must stay below the largest finite E4M3 value (448):
+// a row more than kGrowth above m (256 * 2^0.75 = 430.5) moves m to the page
+// max + kHeadroom, so that later pages rarely move it again.
+constexpr float kGrowth = 0.75f;
+constexpr float kHeadroom = 1.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1 KB alignment");
-static_assert(kOffKRaw % 16 == 0 && kOffVRaw % 16 == 0 && kHalfBytes % 16 == 0, "bulk copy alignment");
-static_assert(kOffMerge % 16 == 0, "alignment");
+static_assert(kOffRaw % 16 == 0 && kHeadBytes % 16 == 0, "bulk copy alignment");
+static_assert(kOffVs - kOffVc == kOffKs - kOffKc, "K and V halves share one layout");
 
 size_t attn_smem_bytes(int n_seqs) { return 1024 + kOffQsl + 4 * (size_t)(n_seqs + 1); }
 
@@ -168,8 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   const WaitCtl wc{s_abort, p.wait_ns};
-  int* s_issued_k = reinterpret_cast<int*>(smem + kOffMisc + 8);
-  int* s_issued_v = reinterpret_cast<int*>(smem + kOffMisc + 12);
+  int* s_issued = reinterpret_cast<int*>(smem + kOffMisc + 8);
   uint2* s_tab = reinterpret_cast<uint2*>(smem + kOffTab);
   int* s_qsl = reinterpret_cast<int*>(smem + kOffQsl);
   auto rec = [&](int slot) { return reinterpret_cast<ItemRec*>(smem + kOffRec + 256 * slot); };
@@ -183,28 +173,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   build_dequant_table(s_tab, tid, kThreads);
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kKrFull + i), 1);
-      mbar_init(bar(kKrEmpty + i), 4 * kConvSets);
-      mbar_init(bar(kVrFull + i), 1);
-      mbar_init(bar(kVrEmpty + i), 4 * kConvSets);
+      mbar_init(bar(kRawFull + i), 1);
+      mbar_init(bar(kRawEmpty + i), 4);  // the 4 warps of the converting group
     }
-    for (int i = 0; i < kK8Slots; ++i) {
-      mbar_init(bar(kK8Full + i), 4 * kConvSets);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(bar(kK8Full + i), 4);
       mbar_init(bar(kK8Empty + i), 1);
+      mbar_init(bar(kV8Full + i), 4);
+      mbar_init(bar(kPFull + i), 4);
+      mbar_init(bar(kPVDone + i), 1);
     }
-    for (int i = 0; i < kSets; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSFull + i), 1);
       mbar_init(bar(kSEmpty + i), 4);
-    }
-    for (int i = 0; i < kMergeBufs; ++i) {
-      mbar_init(bar(kMergeFull + i), 4);
-      mbar_init(bar(kMergeEmpty + i), 4);
-    }
-    for (int i = 0; i < kV8Tiles; ++i) mbar_init(bar(kV8Full + i), 4 * kConvSets);
-    for (int i = 0; i < kPO; ++i) {
-      mbar_init(bar(kPFull + i), 4);
-      mbar_init(bar(kOFull + i), 1);
-      mbar_init(bar(kOEmpty + i), 4);
+      mbar_init(bar(kOFree + i), 4);
     }
     for (int i = 0; i < kRecs; ++i) {
       mbar_init(bar(kRecFull + i), 1);
@@ -213,12 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
     mbar_init(bar(kDone), 1);
     mbar_init(bar(kDone + 1), 1);
     *s_abort = 0;
-    *s_issued_k = 0;
-    *s_issued_v = 0;
+    *s_issued = 0;
     fence_barrier_init();
   }
   // zero the Q tiles and the P tiles (rows that stay zero pad N to 16)
-  for (int i = tid; i < (kRecs + kPO) * 2048 / 16; i += kThreads)
+  for (int i = tid; i < (kRecs + kSlots) * 2048 / 16; i += kThreads)
     reinterpret_cast<uint4*>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
   // q_start_loc does not come from the previous kernel
   for (int i = tid; i <= p.n_seqs; i += kThreads) s_qsl[i] = p.q_start_loc[i];
@@ -296,10 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       if (lane == 0) mbar_arrive(bar(kRecFull + slot));
     }
   } else if (warp == 1) {
-    // ---------------- TMA producer: K and V halves of every page -------------------------
+    // ---------------- TMA producer: one copy per page (K and V halves) -----------------
     if (lane == 0) {
-      int e = 0, st = 0;
-      uint32_t ph = 0;  // ring stage of page e and its phase parity
+      int e = 0;
       bool ok = true;
       for (int k = 0; ok && k < n_mine; ++k) {
         const int slot = k % kRecs;
@@ -308,26 +288,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const int n = r->n_pg;
         const uint8_t* head = p.kv_pool + (size_t)r->kvh * kHeadBytes;
         for (int i = 0; i < n; ++i, ++e) {
-          const uint8_t* src = head + (size_t)r->phys[i] * kKvPageBytes;
-          if (!mbar_wait(bar(kKrEmpty + st), ph ^ 1, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(kKrFull + st), kHalfBytes);
-          bulk_g2s(sbase + kOffKRaw + st * kHalfBytes, src, kHalfBytes, bar(kKrFull + st));
-          *s_issued_k = e + 1;
-          if (!mbar_wait(bar(kVrEmpty + st), ph ^ 1, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(kVrFull + st), kHalfBytes);
-          bulk_g2s(sbase + kOffVRaw + st * kHalfBytes, src + kHalfBytes, kHalfBytes, bar(kVrFull + st));
-          *s_issued_v = e + 1;
-          if (++st == kStages) {
-            st = 0;
-            ph ^= 1;
-          }
+          const int st = e % kStages;
+          if (!mbar_wait(bar(kRawEmpty + st), ((e / kStages) & 1) ^ 1, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(kRawFull + st), kHeadBytes);
+          bulk_g2s(sbase + kOffRaw + st * kHeadBytes, head + (size_t)r->phys[i] * kKvPageBytes, kHeadBytes,
+                   bar(kRawFull + st));
+          *s_issued = e + 1;
         }
         if (ok) mbar_arrive(bar(kRecEmpty + slot));
       }
     }
     __syncwarp();
-  }
-  else if (warp == 2) {
+  } else if (warp == 2) {
     // ---------------- QK issuer ---------------------------------------------------------------
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_e4m3(128, 16);
@@ -339,9 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const int n = rec(slot)->n_pg;
         const uint64_t bdesc = umma_desc_sw128(sbase + kOffQ + slot * 2048);
         for (int i = 0; i < n; ++i, ++e) {
-          const unsigned ue = e;
-          const int sl = ue % kSets, ph = (ue / kSets) & 1, ks = ue % kK8Slots, kph = (ue / kK8Slots) & 1;
-          if (!mbar_wait(bar(kK8Full + ks), kph, wc) || !mbar_wait(bar(kSEmpty + sl), ph ^ 1, wc)) {
+          const int ks = e % kSlots, kph = (e / kSlots) & 1, sl = e & 1, sph = (e >> 1) & 1;
+          if (!mbar_wait(bar(kK8Full + ks), kph, wc) || !mbar_wait(bar(kSEmpty + sl), sph ^ 1, wc)) {
             ok = false;
             break;
           }
@@ -364,18 +335,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
     // ---------------- PV issuer ---------------------------------------------------------------
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_e4m3_amn_bmn(128, 16);
-      int e = 0;
+      int e = 0, ni = 0;  // ni: items with pages so far (O buffer ni & 1)
       bool ok = true;
       for (int k = 0; ok && k < n_mine; ++k) {
         const int slot = k % kRecs;
         if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc)) break;
         const int n = rec(slot)->n_pg;
         mbar_arrive(bar(kRecEmpty + slot));  // nothing else of the record is needed
+        if (n == 0) continue;
+        const int ob = ni & 1;
+        // O buffer ob is free once the softmax has read item ni - 2's output from it
+        if (ni >= 2 && !mbar_wait(bar(kOFree + ob), ((ni >> 1) - 1) & 1, wc)) break;
         for (int i = 0; i < n; ++i, ++e) {
-          const unsigned ue = e;
-          const int v = ue % kV8Tiles, vph = (ue / kV8Tiles) & 1, po = ue % kPO, pph = (ue / kPO) & 1;
-          if (!mbar_wait(bar(kV8Full + v), vph, wc) || !mbar_wait(bar(kPFull + po), pph, wc) ||
-              !mbar_wait(bar(kOEmpty + po), pph ^ 1, wc)) {
+          const int v = e % kSlots, vph = (e / kSlots) & 1;
+          if (!mbar_wait(bar(kV8Full + v), vph, wc) || !mbar_wait(bar(kPFull + v), vph, wc)) {
             ok = false;
             break;
           }
@@ -388,43 +361,36 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
             // 32 tokens of one MMA are 512 bytes
             const uint64_t adesc =
                 umma_desc_sw128_lbo_sbo(sbase + kOffV8 + v * kTileBytes + kk * 4096, 1024, 1024);
-            const uint64_t bdesc = umma_desc_noswz_lbo_sbo(sbase + kOffP + po * 2048 + kk * 512, 128, 128);
-            umma_e4m3(tmem + kTmO + 16 * po, adesc, bdesc, idesc, kk > 0);
+            const uint64_t bdesc = umma_desc_noswz_lbo_sbo(sbase + kOffP + v * 2048 + kk * 512, 128, 128);
+            umma_e4m3(tmem + kTmO + 16 * ob, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          // one commit: page e's O is ready, and its V tile and P tile are free
-          umma_commit(bar(kOFull + po));
+          // page e's V tile and P tile are free (and O holds page e) once this is done
+          umma_commit(bar(kPVDone + v));
         }
+        ++ni;
       }
       umma_commit(bar(kDone + 1));
     }
     __syncwarp();
   } else if (warp >= kWarpConv0) {
-    // ---------------- conversion: K (warps 12 ..) or V (the next 4 kConvSets) --------
-    // thread = token; the kConvSets warps of a token row take its 16-byte code
-    // chunks c = cs * kCh .. cs * kCh + kCh - 1
-    const bool is_k = warp < kWarpConv0 + 4 * kConvSets;
-    constexpr int kCh = 4 / kConvSets;
-    const int cs = ((warp - kWarpConv0) >> 2) % kConvSets;
-    // K warps write TMEM lanes 32 (warp % 4) ..; V warps any order
-    const int tok = 32 * (warp & 3) + lane;
-    const int full0 = is_k ? kKrFull : kVrFull, empty0 = is_k ? kKrEmpty : kVrEmpty;
-    const uint32_t raw0 = is_k ? kOffKRaw : kOffVRaw;
-    // Per-thread offsets of this thread's chunks, fixed for the whole kernel:
-    // code chunk c of token tok sits at position c ^ ((tok >> 1) & 3) of its
-    // 64-byte row (8 consecutive tokens hit 8 bank groups), its two group
-    // scales at [2c][tok] and [2c + 1][tok] after the codes; in the V tile
-    // 16-byte chunk j of row tok sits at position j ^ (tok & 7).
-    uint32_t code_off[kCh], sc_off[kCh], v_off[kCh][2];
+    // ---------------- conversion: group g converts pages e % kGroups == g ------------------
+    const int g = (warp - kWarpConv0) >> 2, quad = warp & 3;
+    const int tok = 32 * quad + lane;  // K rows land in TMEM lanes 32 quad .. (warp % 4 rule)
+    // Per-thread offsets, fixed for the whole kernel: code chunk c of token tok
+    // sits at position c ^ ((tok >> 1) & 3) of its 64-byte row (8 consecutive
+    // tokens hit 8 bank groups), its two group scales at [2c][tok] and
+    // [2c + 1][tok] after the codes; in the V tile 16-byte chunk j of row tok
+    // sits at position j ^ (tok & 7).
+    uint32_t code_off[4], sc_off[4], v_off[4][2];
 #pragma unroll
-    for (int ci = 0; ci < kCh; ++ci) {
-      const int c = cs * kCh + ci;
-      code_off[ci] = tok * 64 + 16 * code_chunk_pos(c, tok);
-      sc_off[ci] = kOffKs + 2 * c * kPageTokens + tok;
-      v_off[ci][0] = tok * 128 + (((2 * c) ^ (tok & 7)) << 4);
-      v_off[ci][1] = tok * 128 + (((2 * c + 1) ^ (tok & 7)) << 4);
+    for (int c = 0; c < 4; ++c) {
+      code_off[c] = tok * 64 + 16 * code_chunk_pos(c, tok);
+      sc_off[c] = (kOffKs - kOffKc) + 2 * c * kPageTokens + tok;
+      v_off[c][0] = tok * 128 + (((2 * c) ^ (tok & 7)) << 4);
+      v_off[c][1] = tok * 128 + (((2 * c + 1) ^ (tok & 7)) << 4);
     }
-    int e = 0, st = 0;
-    uint32_t rph = 0;  // raw ring stage of page e and its phase parity
+    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
+    int e = 0;
     bool ok = true;
     for (int k = 0; ok && k < n_mine; ++k) {
       const int slot = k % kRecs;
@@ -432,150 +398,149 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       const ItemRec* r = rec(slot);
       const int n = r->n_pg;
       for (int i = 0; i < n; ++i, ++e) {
-        // output slot: the K8 buffer e % kK8Slots (freed by its previous QK) or
-        // the V8 tile e % kV8Tiles (freed by the PV of page e - kV8Tiles, whose
-        // commit completes the O barrier of that page: O buffer e % kPO, the
-        // same index since kV8Tiles == kPO)
-        const unsigned ue = e;
-        const int os = is_k ? ue % kK8Slots : ue % kV8Tiles;
-        const uint32_t oph = is_k ? (ue / kK8Slots) & 1 : (ue / kV8Tiles) & 1;
-        bool got = warp_wait(bar(full0 + st), rph, wc);
-        if (got) {
-          if (is_k) got = warp_wait(bar(kK8Empty + os), oph ^ 1, wc);
-          else if (e >= kV8Tiles) got = warp_wait(bar(kOFull + os), oph ^ 1, wc);
+        if (e % kGroups != g) continue;
+        const int st = e % kStages, sl = e % kSlots;
+        const uint32_t sph = (e / kSlots) & 1;
+        // the raw page, and K8 slot sl (free once QK of page e - kSlots is done)
+        if (!warp_wait(bar(kRawFull + st), (e / kStages) & 1, wc) || !warp_wait(bar(kK8Empty + sl), sph ^ 1, wc)) {
+          ok = false;
+          break;
         }
-        if (!got) {
+        const uint8_t* raw = smem + kOffRaw + st * kHeadBytes;
+        uint32_t o[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) convert_chunk(raw + kOffKc + code_off[c], raw + kOffKc + sc_off[c], s_tab, o + 8 * c);
+        // K: row tok of A in TMEM, columns 32 sl + 8c .. + 7 = channels 32c .. 32c + 31
+        // (rows past the query position stay as converted: the softmax masks them)
+        tmem_st32(trow + 32 * sl, o);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kK8Full + sl));
+        // V tile sl is free once PV of page e - kSlots is done
+        if (e >= kSlots && !warp_wait(bar(kPVDone + sl), sph ^ 1, wc)) {
           ok = false;
           break;
         }
         // tokens after the query position (only in the recent block) become zeros
         const int valid = r->valid[i];
-        const bool full = valid >= 32 * (warp & 3) + 32;  // warp-uniform
+        const bool full = valid >= 32 * quad + 32;  // warp-uniform
         const bool live = tok < valid;
-        const uint8_t* raw = smem + raw0 + st * kHalfBytes;
-        // K: row tok of A in TMEM, columns 32 os + 8c .. + 7 = channels 32c .. 32c + 31
-        const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * os;
-        uint8_t* dst = smem + kOffV8 + os * kTileBytes;
+        uint8_t* dst = smem + kOffV8 + sl * kTileBytes;
 #pragma unroll
-        for (int ci = 0; ci < kCh; ++ci) {
-          uint32_t o[8];
-          convert_chunk(raw + code_off[ci], raw + sc_off[ci], s_tab, o);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t* oc = o + 8 * c;
+          convert_chunk(raw + kOffVc + code_off[c], raw + kOffVc + sc_off[c], s_tab, oc);
           if (!full) {
 #pragma unroll
-            for (int x = 0; x < 8; ++x) o[x] = live ? o[x] : 0u;
+            for (int x = 0; x < 8; ++x) oc[x] = live ? oc[x] : 0u;
           }
-          if (is_k) {
-            tmem_st8(ta + 8 * (cs * kCh + ci), o);
-          } else {
-            *reinterpret_cast<uint4*>(dst + v_off[ci][0]) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(dst + v_off[ci][1]) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
+          *reinterpret_cast<uint4*>(dst + v_off[c][0]) = make_uint4(oc[0], oc[1], oc[2], oc[3]);
+          *reinterpret_cast<uint4*>(dst + v_off[c][1]) = make_uint4(oc[4], oc[5], oc[6], oc[7]);
         }
-        if (is_k) {
-          tmem_wait_st();
-          tc_fence_before();
-        } else {
-          fence_proxy_async_smem();
-        }
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (is_k) mbar_arrive(bar(kK8Full + os));
-          else mbar_arrive(bar(kV8Full + os));
-          mbar_arrive(bar(empty0 + st));
-        }
-        if (++st == kStages) {
-          st = 0;
-          rph ^= 1;
+          mbar_arrive(bar(kV8Full + sl));
+          mbar_arrive(bar(kRawEmpty + st));
         }
       }
       if (ok && lane == 0) mbar_arrive(bar(kRecEmpty + slot));
     }
-  }
-  else if (warp >= 4) {
-    // ---------------- softmax: set s = warps 4 + 4 s .. 7 + 4 s ------------------------
-    // set s takes the pages with e % kSets == s; warp w reads TMEM lanes 32 (w % 4) ..:
-    // row = token of S, channel of O
-    const int set = (warp - 4) >> 2, quad = warp & 3, row = 32 * quad + lane;
+  } else if (warp >= 4) {
+    // ---------------- softmax: warps 4-7 -------------------------------------------------------
+    // warp w reads TMEM lanes 32 (w % 4) ..: row = token of S, channel of O
+    const int quad = warp & 3, row = 32 * quad + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
-    const int nb = 1 + set;  // named barrier of the set
-    float* red = reinterpret_cast<float*>(smem + kOffRed) + set * 32;   // [2][4 warps][4 heads]
-    float* redl = reinterpret_cast<float*>(smem + kOffRedL) + set * 16;  // [4 warps][4 heads]
-    int e0 = 0;  // page number of the item's first page
+    constexpr int nb = 1;  // named barrier of the four warps
+    float* red = reinterpret_cast<float*>(smem + kOffRed);    // [4 warps][4 heads]
+    float* redl = reinterpret_cast<float*>(smem + kOffRedL);  // [4 warps][4 heads]
+    int e = 0, ni = 0;
     bool ok = true;
     for (int k = 0; ok && k < n_mine; ++k) {
       const int slot = k % kRecs;
       if (named_barrier_or(nb, 128, !warp_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc))) break;
       const ItemRec* r = rec(slot);
       const int n = r->n_pg;
-      float m_run[4], l_run[4], o_run[4], a_prev[4], b_prev[4];
+      const int ob = ni & 1;
+      float m_ref[4], l_run[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        m_run[h] = -INFINITY;
+        m_ref[h] = -INFINITY;
         l_run[h] = 0.f;
-        o_run[h] = 0.f;
-        a_prev[h] = 1.f;
-        b_prev[h] = 0.f;
       }
-      // O of page ef (relative to its page max) -> running state
-      auto fold = [&](int ef) -> bool {
-        const int po = (unsigned)ef % kPO;
-        if (!warp_wait(bar(kOFull + po), ((unsigned)ef / kPO) & 1, wc)) return false;
-        tc_fence_after();
-        float ov[8];
-        tmem_ld8(trow + kTmO + 16 * po, ov);  // columns 0-3: hi terms, 4-7: remainders
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kOEmpty + po));
-#pragma unroll
-        for (int h = 0; h < 4; ++h) o_run[h] = o_run[h] * a_prev[h] + (ov[h] + ov[4 + h]) * b_prev[h];
-        return true;
-      };
-      int e_prev = -1;
-      for (int e = e0 + (set - e0 % kSets + kSets) % kSets; e < e0 + n; e += kSets) {
-        const int ph = ((unsigned)e / kSets) & 1;
-        bool good = warp_wait(bar(kSFull + set), ph, wc);
+      for (int i = 0; i < n; ++i, ++e) {
+        const int sl = e & 1;
+        bool good = warp_wait(bar(kSFull + sl), (e >> 1) & 1, wc);
         float sv[4] = {0.f, 0.f, 0.f, 0.f};
         if (good) {
           tc_fence_after();
-          tmem_ld4(trow + kTmS + 16 * set, sv);
+          tmem_ld4(trow + kTmS + 16 * sl, sv);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kSEmpty + set));
+          if (lane == 0) mbar_arrive(bar(kSEmpty + sl));
         }
-        const bool live = row < r->valid[e - e0];
-        float* rd = red + ph * 16;
-        float x[4], wm[4];
+        const bool live = row < r->valid[i];
+        float x[4];
+        bool over = false;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           x[h] = live ? sv[h] * p.scale_log2 : -INFINITY;
-          wm[h] = warp_max_f32(x[h]);
+          over = over || x[h] > m_ref[h] + kGrowth;
         }
-        if (lane == 0) reinterpret_cast<float4*>(rd)[quad] = make_float4(wm[0], wm[1], wm[2], wm[3]);
-        // page maxima complete; the set's four warps agree on whether to go on
-        if (named_barrier_or(nb, 128, !good || !ok)) {
-          ok = false;
-          break;
-        }
-        float a_cur[4], b_cur[4], v[4];
-        {
-          const float4 r0 = reinterpret_cast<const float4*>(rd)[0], r1 = reinterpret_cast<const float4*>(rd)[1];
-          const float4 r2 = reinterpret_cast<const float4*>(rd)[2], r3 = reinterpret_cast<const float4*>(rd)[3];
+        bool step_ok = true;
+        // a row above the reference (always on the item's first page), or an abort
+        if (named_barrier_or(nb, 128, over || !good || !ok)) {
+          if (named_barrier_or(nb, 128, !good || !ok)) {
+            ok = false;
+            break;
+          }
+          // exact page max per head over the 128 rows
+          float wm[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) wm[h] = warp_max_f32(x[h]);
+          if (lane == 0) reinterpret_cast<float4*>(red)[quad] = make_float4(wm[0], wm[1], wm[2], wm[3]);
+          named_barrier_sync(nb, 128);
+          const float4 r0 = reinterpret_cast<const float4*>(red)[0], r1 = reinterpret_cast<const float4*>(red)[1];
+          const float4 r2 = reinterpret_cast<const float4*>(red)[2], r3 = reinterpret_cast<const float4*>(red)[3];
           const float mps[4] = {fmaxf(fmaxf(r0.x, r1.x), fmaxf(r2.x, r3.x)), fmaxf(fmaxf(r0.y, r1.y), fmaxf(r2.y, r3.y)),
                                 fmaxf(fmaxf(r0.z, r1.z), fmaxf(r2.z, r3.z)), fmaxf(fmaxf(r0.w, r1.w), fmaxf(r2.w, r3.w))};
+          float f[4];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            const float mp = mps[h];
-            // one of the two rescale factors is 1: the running state (a) moves
-            // to the page max when it grows, else the page (b) to the running max
-            const bool grow = mp > m_run[h];
-            const float f = fast_exp2(grow ? m_run[h] - mp : mp - m_run[h]);
-            a_cur[h] = grow ? f : 1.f;
-            b_cur[h] = grow ? 1.f : (mp == -INFINITY ? 0.f : f);
-            m_run[h] = fmaxf(m_run[h], mp);
-            // 256 p relative to the page max (<= 256: exact range of E4M3)
-            v[h] = mp == -INFINITY ? 0.f : fast_exp2(x[h] - mp + 8.f);
-            l_run[h] = l_run[h] * a_cur[h] + v[h] * b_cur[h];
+            // only heads whose page max outgrew the reference move it
+            const float m_new = mps[h] > m_ref[h] + kGrowth ? mps[h] + kHeadroom : m_ref[h];
+            f[h] = m_ref[h] == -INFINITY ? 0.f : fast_exp2(m_ref[h] - m_new);
+            l_run[h] *= f[h];
+            m_ref[h] = m_new;
           }
+          if (i > 0) {
+            // O holds the item's earlier pages relative to the old reference:
+            // once their PVs are done (PV of page e - 1), rescale it in place
+            const int pv = (e - 1) % kSlots;
+            step_ok = warp_wait(bar(kPVDone + pv), ((e - 1) / kSlots) & 1, wc);
+            if (step_ok) {
+              tc_fence_after();
+              float ov[8];
+              tmem_ld8(trow + kTmO + 16 * ob, ov);  // thread = channel: hi terms, then remainders
+              uint32_t ou[8];
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                ou[h] = __float_as_uint(ov[h] * f[h]);
+                ou[4 + h] = __float_as_uint(ov[4 + h] * f[h]);
+              }
+              tmem_st8(trow + kTmO + 16 * ob, ou);
+              tmem_wait_st();
+              tc_fence_before();
+            }
+          }
+        }
+        float v[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          // 256 p relative to the reference (<= 256 * 2^kGrowth < 448)
+          v[h] = x[h] == -INFINITY ? 0.f : fast_exp2(x[h] - m_ref[h] + 8.f);
+          l_run[h] += v[h];
         }
         // 256 p as two E4M3 terms: hi = E4M3(256 p), lo = E4M3(f16(256 p) - hi)
         // (the f16 difference is exact: hi is within a factor of two of 256 p)
@@ -583,30 +548,34 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const uint32_t lo01 = cvt_e4m3x2_f16x2(hsub2_u32(cvt_f16x2_f32(v[1], v[0]), cvt_f16x2_e4m3x2(hi01)));
         const uint32_t lo23 = cvt_e4m3x2_f16x2(hsub2_u32(cvt_f16x2_f32(v[3], v[2]), cvt_f16x2_e4m3x2(hi23)));
         // P tile row = token: bytes 0-3 hi terms of heads 0-3, 4-7 the remainders
-        // (bytes 8-15 stay zero: they pad N to 16)
-        const int po = (unsigned)e % kPO;
-        // P tile po is free once the PV of page e - kPO is done (its O barrier)
-        bool step_ok = warp_wait(bar(kOFull + po), (((unsigned)e / kPO) & 1) ^ 1, wc);
+        // (bytes 8-15 stay zero: they pad N to 16); tile e % kSlots is free once
+        // PV of page e - kSlots is done
+        const int po = e % kSlots;
+        if (step_ok && e >= kSlots) step_ok = warp_wait(bar(kPVDone + po), ((e / kSlots) & 1) ^ 1, wc);
         if (step_ok) {
           *reinterpret_cast<uint2*>(smem + kOffP + po * 2048 + 16 * row) =
               make_uint2(prmt(hi01, hi23, 0x5410u), prmt(lo01, lo23, 0x5410u));
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kPFull + po));
-          if (e_prev >= 0) step_ok = fold(e_prev);
         }
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          a_prev[h] = a_cur[h];
-          b_prev[h] = b_cur[h];
-        }
-        e_prev = e;
         ok = ok && step_ok;  // a failure here ends the loop at the next barrier
       }
-      if (ok && e_prev >= 0) ok = fold(e_prev);
+      // ---- the item's output: O after its last PV, thread = channel ---------------------------
+      float ov[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (ok && n > 0) {
+        const int pv = (e - 1) % kSlots;
+        ok = warp_wait(bar(kPVDone + pv), ((e - 1) / kSlots) & 1, wc);
+        if (ok) {
+          tc_fence_after();
+          tmem_ld8(trow + kTmO + 16 * ob, ov);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kOFree + ob));  // PV of item ni + 2 may overwrite it
+        }
+      }
       const bool aborted = named_barrier_or(nb, 128, !ok || *s_abort != 0);
-      // ---- this set's sum of p over its tokens -------------------------------------------
-      float L[4];
+      // sum of p over the 128 rows, per head
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         float l = l_run[h];
@@ -615,63 +584,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         if (lane == 0) redl[quad * 4 + h] = l;
       }
       named_barrier_sync(nb, 128);
+      const size_t row0 = ((size_t)r->j * p.n_splits + r->split) * kQHeads + r->kvh * kGqa;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) L[h] = aborted ? 0.f : redl[h] + redl[4 + h] + redl[8 + h] + redl[12 + h];
-      // ---- merge the sets' states: sets 1 .. kSets - 1 hand over, set 0 writes ------------
-      const int mph = (k >> 1) & 1;
-      auto merge_buf = [&](int helper) {  // o [4][128], m [4], L [4]
-        return reinterpret_cast<float*>(smem + kOffMerge + (2 * (helper - 1) + (k & 1)) * kMergeBytes);
-      };
-      if (set > 0) {
-        const int mb = 2 * (set - 1) + (k & 1);
-        float* mo = merge_buf(set);
-        if (warp_wait(bar(kMergeEmpty + mb), mph ^ 1, wc)) {
-#pragma unroll
-          for (int h = 0; h < 4; ++h) mo[h * 128 + row] = o_run[h];
-          if (row == 0) {
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              mo[512 + h] = m_run[h];
-              mo[516 + h] = L[h];
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kMergeFull + mb));
-        }
-      } else {
-        bool got = true;
-#pragma unroll
-        for (int hs = 1; hs < kSets; ++hs)
-          got = warp_wait(bar(kMergeFull + 2 * (hs - 1) + (k & 1)), mph, wc) && got;
-        const size_t row0 = ((size_t)r->j * p.n_splits + r->split) * kQHeads + r->kvh * kGqa;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          float m = m_run[h];
-#pragma unroll
-          for (int hs = 1; hs < kSets; ++hs) m = fmaxf(m, got ? merge_buf(hs)[512 + h] : -INFINITY);
-          const float w0 = (m_run[h] == -INFINITY || L[h] == 0.f) ? 0.f : fast_exp2(m_run[h] - m);
-          float Lm = L[h] * w0, om = o_run[h] * w0;
-#pragma unroll
-          for (int hs = 1; hs < kSets; ++hs) {
-            const float* mo = merge_buf(hs);
-            const float m1 = got ? mo[512 + h] : -INFINITY, L1 = got ? mo[516 + h] : 0.f;
-            const float w1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : fast_exp2(m1 - m);
-            Lm += L1 * w1;
-            om += (got ? mo[h * 128 + row] : 0.f) * w1;
-          }
-          const bool nonempty = !aborted && got && Lm > 0.f;
-          p.o_part[(row0 + h) * kHeadDim + row] = nonempty ? om / Lm * p.out_scale : 0.f;
-          if (row == 0) p.lse_part[row0 + h] = nonempty ? (m + log2f(Lm) - 8.f) * kLn2 : -INFINITY;
-        }
-        __syncwarp();
-        if (lane == 0 && got) {
-#pragma unroll
-          for (int hs = 1; hs < kSets; ++hs) mbar_arrive(bar(kMergeEmpty + 2 * (hs - 1) + (k & 1)));
-        }
+      for (int h = 0; h < 4; ++h) {
+        const float L = aborted ? 0.f : redl[h] + redl[4 + h] + redl[8 + h] + redl[12 + h];
+        const bool nonempty = !aborted && n > 0 && L > 0.f;
+        p.o_part[(row0 + h) * kHeadDim + row] = nonempty ? (ov[h] + ov[4 + h]) / L * p.out_scale : 0.f;
+        if (row == 0) p.lse_part[row0 + h] = nonempty ? (m_ref[h] + log2f(L) - 8.f) * kLn2 : -INFINITY;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kRecEmpty + slot));
-      e0 += n;
+      if (n > 0) ++ni;
       ok = !aborted;
     }
   }
@@ -685,14 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
     mbar_wait_drain(bar(kDone + 1), 0, p.wait_ns);
     if (*s_abort) {
       set_status(p.status, MSA_STATUS_TIMEOUT);
-      // bounded drain of the copies that may still be landing: the last kStages
-      // issued on each ring (every earlier one was consumed before its stage was
+      // bounded drain of the copies that may still be landing: the last
+      // kStages issued (every earlier one was consumed before its stage was
       // refilled)
-      const int nk = *s_issued_k, nv = *s_issued_v;
-      for (int e = max(0, nk - kStages); e < nk; ++e)
-        mbar_wait_drain(bar(kKrFull + e % kStages), (e / kStages) & 1, p.wait_ns);
-      for (int e = max(0, nv - kStages); e < nv; ++e)
-        mbar_wait_drain(bar(kVrFull + e % kStages), (e / kStages) & 1, p.wait_ns);
+      const int ni = *s_issued;
+      for (int e = max(0, ni - kStages); e < ni; ++e)
+        mbar_wait_drain(bar(kRawFull + e % kStages), (e / kStages) & 1, p.wait_ns);
     }
   }
   __syncthreads();
