@@ -5,8 +5,8 @@
 // both data movement and resource waits": fusing the QKV projection with the
 // normalisation, RoPE and cache insertion avoids writing the full intermediate
 // tensor to HBM and reading it back.  Here the projection's accumulators never
-// leave the SM: each CTA computes one tile of 128 tokens x one head (128
-// output columns) on the tensor core and its epilogue finishes that head.
+// leave the SM: each CTA computes one tile of 128 tokens x two heads (256
+// output columns) on the tensor core and its epilogue finishes both heads.
 //
 // Output heads of the projection (columns of W, 128 each): 16 query heads,
 // 4 key heads, 4 value heads, 1 index-key head.  Per token and head:
@@ -18,14 +18,16 @@
 //
 // Tile pipeline (one CTA per tile, two per SM):
 //   warp 0      TMA producer: per 64-column K chunk, a 128 x 64 bf16 tile of x
-//               and of W (cp.async.bulk.tensor, 128-byte swizzle) into a
-//               3-stage ring;
+//               and two of W (the two heads; cp.async.bulk.tensor, 128-byte
+//               swizzle) into a 2-stage ring;
 //   warp 1      MMA issuer: 4 x tcgen05.mma kind::f16 (bf16 in, fp32 out;
-//               M = 128 tokens, N = 128 columns, K = 16) per chunk, the
-//               accumulator in tensor memory;
-//   warps 2-5   epilogue: thread = token row, all 128 columns in registers:
-//               RMS norm and RoPE are thread-local, so is the NVFP4 quantiser
-//               (a 16-channel group lives in one thread).
+//               M = 128 tokens, N = 256 columns, K = 16) per chunk, the
+//               accumulator in tensor memory.  One tcgen05.mma costs its
+//               issuing thread about 200 cycles whatever its N, so the widest N
+//               does the most work per instruction;
+//   warps 2-5   epilogue: thread = token row, one head's 128 columns at a time
+//               in registers: RMS norm and RoPE are thread-local, so is the
+//               NVFP4 quantiser (a 16-channel group lives in one thread).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,12 +37,13 @@ namespace msa {
 namespace {
 
 constexpr int kQkvThreads = 192;
-constexpr int kQkvStages = 3;
+constexpr int kQkvStages = 2;
+constexpr int kHeadsPerCta = 2;               // N = 256
 constexpr int kChunk = 64;                    // bf16 elements of K per stage (128 bytes)
-constexpr int kTileBytes = 128 * kChunk * 2;  // 16 KB per operand tile
-constexpr int kOffA = 0;
-constexpr int kOffB = kQkvStages * kTileBytes;
-constexpr int kOffGamma = 2 * kQkvStages * kTileBytes;  // 3 x 128 floats
+constexpr int kTileBytes = 128 * kChunk * 2;  // 16 KB per 128-row operand tile
+constexpr int kOffA = 0;                                          // kQkvStages x 16 KB of x
+constexpr int kOffB = kQkvStages * kTileBytes;                    // kQkvStages x 32 KB of W (two heads)
+constexpr int kOffGamma = kOffB + kQkvStages * kHeadsPerCta * kTileBytes;  // 3 x 128 floats
 constexpr int kOffBarQ = kOffGamma + 3 * 128 * 4;
 constexpr int kQkvSmem = kOffBarQ + 8 * (2 * kQkvStages + 1) + 16;  // + tmem slot, abort, copies issued
 constexpr int kHeadsOut = kQHeads + 2 * kKvHeads + 1;  // 25
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kQkvThreads, 2) qkv_fused_kernel(const __grid_
   float* s_gamma = reinterpret_cast<float*>(smem + kOffGamma);
   const WaitCtl wc{s_abort, p.wait_ns};
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int mt = blockIdx.x, hd = blockIdx.y;  // 128-token tile, output head
+  const int mt = blockIdx.x, hd0 = kHeadsPerCta * blockIdx.y;  // 128-token tile, first output head
   const int n_chunks = p.d_model / kChunk;
 
   if (tid == 0) {
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(kQkvThreads, 2) qkv_fused_kernel(const __grid_
     s_gamma[128 + tid] = p.gamma_k[tid];
     s_gamma[256 + tid] = p.gamma_idx[tid];
   }
-  if (warp == 1) tmem_alloc(smem_u32(s_tmem), 128);
+  if (warp == 1) tmem_alloc(smem_u32(s_tmem), 128 * kHeadsPerCta);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -164,22 +167,27 @@ __global__ void __launch_bounds__(kQkvThreads, 2) qkv_fused_kernel(const __grid_
       for (int kc = 0; kc < n_chunks; ++kc) {
         const int st = kc % kQkvStages;
         if (!mbar_wait(empty(st), ((kc / kQkvStages) & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(full(st), 2 * kTileBytes);
+        // (rows past either matrix, the token tail or the 26th head, read as zeros)
+        mbar_arrive_expect_tx(full(st), (1 + kHeadsPerCta) * kTileBytes);
         tma_load_2d(sbase + kOffA + st * kTileBytes, &p.tmap_x, kc * kChunk, mt * 128, full(st));
-        tma_load_2d(sbase + kOffB + st * kTileBytes, &p.tmap_w, kc * kChunk, hd * 128, full(st));
+#pragma unroll
+        for (int h = 0; h < kHeadsPerCta; ++h)
+          tma_load_2d(sbase + kOffB + (st * kHeadsPerCta + h) * kTileBytes, &p.tmap_w, kc * kChunk,
+                      (hd0 + h) * 128, full(st));
         *s_issued = kc + 1;
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(128, 128);
+      const uint32_t idesc = umma_idesc_bf16(128, 128 * kHeadsPerCta);
       for (int kc = 0; kc < n_chunks; ++kc) {
         const int st = kc % kQkvStages;
         if (!mbar_wait(full(st), (kc / kQkvStages) & 1, wc)) break;
         tc_fence_after();
         const uint64_t a = umma_desc_sw128(sbase + kOffA + st * kTileBytes);
-        const uint64_t b = umma_desc_sw128(sbase + kOffB + st * kTileBytes);
+        // the two heads' W tiles are consecutive: one K-major operand of 256 rows
+        const uint64_t b = umma_desc_sw128(sbase + kOffB + st * kHeadsPerCta * kTileBytes);
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // K = 16 bf16 = 32 bytes per MMA: +2 in the encoded address
           umma_bf16(tmem, a + 2 * k, b + 2 * k, idesc, (kc | k) != 0);
@@ -194,101 +202,106 @@ __global__ void __launch_bounds__(kQkvThreads, 2) qkv_fused_kernel(const __grid_
     const int token = mt * 128 + row;
     const bool ok = mbar_wait(done, 0, wc);
     tc_fence_after();
-    float y[128];
-    if (ok) {
-      uint32_t v[128];
-      const uint32_t ta = tmem + ((uint32_t)(32 * quad) << 16);
-      tmem_ld32x32b_x32(ta, v);
-      tmem_ld32x32b_x32(ta + 32, v + 32);
-      tmem_ld32x32b_x32(ta + 64, v + 64);
-      tmem_ld32x32b_x32(ta + 96, v + 96);
-      tmem_wait_ld();
+    // the CTA's heads one after the other (128 accumulator columns each)
+    for (int h = 0; h < kHeadsPerCta; ++h) {
+      const int hd = hd0 + h;
+      if (hd >= kHeadsOut) break;
+      float y[128];
+      if (ok) {
+        uint32_t v[128];
+        const uint32_t ta = tmem + ((uint32_t)(32 * quad) << 16) + 128 * h;
+        tmem_ld32x32b_x32(ta, v);
+        tmem_ld32x32b_x32(ta + 32, v + 32);
+        tmem_ld32x32b_x32(ta + 64, v + 64);
+        tmem_ld32x32b_x32(ta + 96, v + 96);
+        tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 128; ++i) y[i] = __uint_as_float(v[i]);
-    }
-    tc_fence_before();
-    const bool is_q = hd < kQHeads, is_k = hd >= kQHeads && hd < kQHeads + kKvHeads;
-    const bool is_v = hd >= kQHeads + kKvHeads && hd < kQHeads + 2 * kKvHeads, is_idx = hd == kHeadsOut - 1;
-    if (ok && token < p.n_tokens) {
-      if (!is_v) {
-        // RMS norm over the head's 128 channels, times the head type's gamma
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < 128; ++i) ss = fmaf(y[i], y[i], ss);
-        const float rn = 1.0f / sqrtf(ss / 128.0f + p.eps);
-        const float* gm = s_gamma + (is_q ? 0 : is_k ? 128 : 256);
-#pragma unroll
-        for (int i = 0; i < 128; ++i) y[i] = y[i] * rn * gm[i];
-        // RoPE, channel pairs (i, i + 64) rotated by the angle of pair i at the
-        // token's position
-        const int pos = p.positions[token];
-        if (pos >= 0 && pos < p.max_pos) {
-          const float4* cs = reinterpret_cast<const float4*>(p.cos_sin + (size_t)pos * 128);
-#pragma unroll
-          for (int i4 = 0; i4 < 16; ++i4) {
-            const float4 c = __ldg(cs + i4), s = __ldg(cs + 16 + i4);
-            const float cc[4] = {c.x, c.y, c.z, c.w}, sn[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int i = 4 * i4 + u;
-              const float a = y[i], b = y[i + 64];
-              y[i] = a * cc[u] - b * sn[u];
-              y[i + 64] = b * cc[u] + a * sn[u];
-            }
-          }
-        } else if (lane == 0) {
-          set_status(p.status, MSA_STATUS_BAD_SEQ);
-        }
+        for (int i = 0; i < 128; ++i) y[i] = __uint_as_float(v[i]);
       }
-      if (p.y_out) {
-        float4* dst = reinterpret_cast<float4*>(p.y_out + ((size_t)token * kHeadsOut + hd) * 128);
+      const bool is_q = hd < kQHeads, is_k = hd >= kQHeads && hd < kQHeads + kKvHeads;
+      const bool is_v = hd >= kQHeads + kKvHeads && hd < kQHeads + 2 * kKvHeads, is_idx = hd == kHeadsOut - 1;
+      if (ok && token < p.n_tokens) {
+        if (!is_v) {
+          // RMS norm over the head's 128 channels, times the head type's gamma
+          float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-      }
-      if (is_q) {
-        uint8_t* dst = p.q8 + ((size_t)token * kQHeads + hd) * 128;
+          for (int i = 0; i < 128; ++i) ss = fmaf(y[i], y[i], ss);
+          const float rn = 1.0f / sqrtf(ss / 128.0f + p.eps);
+          const float* gm = s_gamma + (is_q ? 0 : is_k ? 128 : 256);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
+          for (int i = 0; i < 128; ++i) y[i] = y[i] * rn * gm[i];
+          // RoPE, channel pairs (i, i + 64) rotated by the angle of pair i at the
+          // token's position
+          const int pos = p.positions[token];
+          if (pos >= 0 && pos < p.max_pos) {
+            const float4* cs = reinterpret_cast<const float4*>(p.cos_sin + (size_t)pos * 128);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t lo = f32x2_to_e4m3x2(y[16 * c + 4 * u], y[16 * c + 4 * u + 1]);
-            const uint32_t hi = f32x2_to_e4m3x2(y[16 * c + 4 * u + 2], y[16 * c + 4 * u + 3]);
-            w[u] = canon_zero(lo & 0xFF) | (canon_zero(lo >> 8) << 8) | (canon_zero(hi & 0xFF) << 16) |
-                   (canon_zero(hi >> 8) << 24);
-          }
-          *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      } else {
-        const int64_t slot = p.slot_mapping[token];
-        const int64_t page = slot >= 0 ? slot / kPageTokens : -1;
-        const int off = slot >= 0 ? (int)(slot % kPageTokens) : 0;
-        if (slot >= 0 && page >= p.n_pages) {
-          set_status(p.status, MSA_STATUS_BAD_SLOT);
-        } else if (slot >= 0) {
-          if (is_idx) {
-            uint8_t* dst = p.idx_pool + (size_t)page * kIdxPageBytes + off * kIdxDim;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              uint32_t w[4];
+            for (int i4 = 0; i4 < 16; ++i4) {
+              const float4 c = __ldg(cs + i4), s = __ldg(cs + 16 + i4);
+              const float cc[4] = {c.x, c.y, c.z, c.w}, sn[4] = {s.x, s.y, s.z, s.w};
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                const uint32_t lo = f32x2_to_e4m3x2(y[16 * c + 4 * u], y[16 * c + 4 * u + 1]);
-                const uint32_t hi = f32x2_to_e4m3x2(y[16 * c + 4 * u + 2], y[16 * c + 4 * u + 3]);
-                w[u] = canon_zero(lo & 0xFF) | (canon_zero(lo >> 8) << 8) | (canon_zero(hi & 0xFF) << 16) |
-                       (canon_zero(hi >> 8) << 24);
+                const int i = 4 * i4 + u;
+                const float a = y[i], b = y[i + 64];
+                y[i] = a * cc[u] - b * sn[u];
+                y[i + 64] = b * cc[u] + a * sn[u];
               }
-              *reinterpret_cast<uint4*>(dst + ((c ^ (off & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-          } else {
-            const int g = hd - (is_k ? kQHeads : kQHeads + kKvHeads);
-            uint8_t* head = p.kv_pool + (size_t)page * kKvPageBytes + g * kHeadBytes;
-            store_nvfp4_row(y, is_k ? p.s_enc_k : p.s_enc_v, head, is_k ? kOffKc : kOffVc,
-                            is_k ? kOffKs : kOffVs, off);
+          } else if (lane == 0) {
+            set_status(p.status, MSA_STATUS_BAD_SEQ);
+          }
+        }
+        if (p.y_out) {
+          float4* dst = reinterpret_cast<float4*>(p.y_out + ((size_t)token * kHeadsOut + hd) * 128);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+        }
+        if (is_q) {
+          uint8_t* dst = p.q8 + ((size_t)token * kQHeads + hd) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t lo = f32x2_to_e4m3x2(y[16 * c + 4 * u], y[16 * c + 4 * u + 1]);
+              const uint32_t hi = f32x2_to_e4m3x2(y[16 * c + 4 * u + 2], y[16 * c + 4 * u + 3]);
+              w[u] = canon_zero(lo & 0xFF) | (canon_zero(lo >> 8) << 8) | (canon_zero(hi & 0xFF) << 16) |
+                     (canon_zero(hi >> 8) << 24);
+            }
+            *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          const int64_t slot = p.slot_mapping[token];
+          const int64_t page = slot >= 0 ? slot / kPageTokens : -1;
+          const int off = slot >= 0 ? (int)(slot % kPageTokens) : 0;
+          if (slot >= 0 && page >= p.n_pages) {
+            set_status(p.status, MSA_STATUS_BAD_SLOT);
+          } else if (slot >= 0) {
+            if (is_idx) {
+              uint8_t* dst = p.idx_pool + (size_t)page * kIdxPageBytes + off * kIdxDim;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const uint32_t lo = f32x2_to_e4m3x2(y[16 * c + 4 * u], y[16 * c + 4 * u + 1]);
+                  const uint32_t hi = f32x2_to_e4m3x2(y[16 * c + 4 * u + 2], y[16 * c + 4 * u + 3]);
+                  w[u] = canon_zero(lo & 0xFF) | (canon_zero(lo >> 8) << 8) | (canon_zero(hi & 0xFF) << 16) |
+                         (canon_zero(hi >> 8) << 24);
+                }
+                *reinterpret_cast<uint4*>(dst + ((c ^ (off & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            } else {
+              const int g = hd - (is_k ? kQHeads : kQHeads + kKvHeads);
+              uint8_t* head = p.kv_pool + (size_t)page * kKvPageBytes + g * kHeadBytes;
+              store_nvfp4_row(y, is_k ? p.s_enc_k : p.s_enc_v, head, is_k ? kOffKc : kOffVc,
+                              is_k ? kOffKs : kOffVs, off);
+            }
           }
         }
       }
     }
+    tc_fence_before();
   }
 
   // ---- teardown ------------------------------------------------------------------
@@ -309,7 +322,7 @@ __global__ void __launch_bounds__(kQkvThreads, 2) qkv_fused_kernel(const __grid_
   }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 128 * kHeadsPerCta);
   }
 }
 
@@ -397,7 +410,7 @@ cudaError_t launch_qkv_fused(const msa_cache* c, const void* x, const void* w, i
   qp.y_out = y_out;
   qp.status = c->status;
   qp.wait_ns = launch_settings().wait_ns;
-  const dim3 grid((n_tokens + 127) / 128, kHeadsOut);
+  const dim3 grid((n_tokens + 127) / 128, (kHeadsOut + kHeadsPerCta - 1) / kHeadsPerCta);
   qkv_fused_kernel<<<grid, kQkvThreads, kQkvSmem + 1024, stream>>>(qp);
   return cudaGetLastError();
 }
