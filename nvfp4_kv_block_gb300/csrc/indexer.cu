@@ -73,14 +73,20 @@ constexpr int kOffPrefix = kOffMisc + 32;  // misc: tmem slot, abort, page range
 // page prefix (n_seqs + 1), seq_lens (n_seqs), q_start_loc (n_seqs + 1).
 size_t scan_smem_bytes(int n_seqs) { return 1024 + kOffPrefix + 20 * (size_t)n_seqs + 16; }
 
-// Relative cost of scanning one page for a sequence with n_q query tokens: a
-// fixed part per pass of up to 8 tokens (the page's bytes) plus the epilogue's
-// per-token part.  With two MMA issuers and three epilogue sets the scan of the
-// ragged batch streams its pages at the DRAM's pace, so the per-token part is
-// small: 28, 48 and 96 for the fixed part measured within 1.5% of each other.
-constexpr int kPassCost = 64;
+// Cost model of the scan, fitted to per-CTA scan times on the ragged batch
+// (152 partitions, contiguous and permuted page layouts agreeing): the cost of
+// one page for a pass of n = 1..8 query tokens (flat while the page's bytes
+// set the pace, rising once the epilogue's per-token work does), and the cost
+// of starting a segment (a sequence's pass: new query tile, pipeline refill),
+// about six pages.  Weights in thousandths of a one-token page.
+__constant__ int kPassPageCost[kNqMax + 1] = {0, 1000, 1009, 1017, 1022, 1038, 1072, 1094, 1139};
+constexpr long long kSegmentCost = 6000;
 __device__ __forceinline__ long long page_weight(int n_q) {
-  return (long long)((n_q + kNqMax - 1) / kNqMax) * kPassCost + n_q;
+  return (long long)(n_q / kNqMax) * kPassPageCost[kNqMax] + kPassPageCost[n_q % kNqMax];
+}
+// Weight of a sequence: its pages, plus one segment start per pass.
+__device__ __forceinline__ long long seq_weight(int pages, int n_q) {
+  return pages > 0 ? (long long)((n_q + kNqMax - 1) / kNqMax) * kSegmentCost + pages * page_weight(n_q) : 0;
 }
 
 // Blocks a sequence's query tokens compete over: 0..r_last-1, r_last =
@@ -177,7 +183,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
       if (!s.ok && blockIdx.x == 0) set_status(p.status, MSA_STATUS_BAD_SEQ);
       const int pages = scan_pages(p, s);
       lp += pages;
-      lw += pages * page_weight(s.n_q);
+      lw += seq_weight(pages, s.n_q);
     }
     // block-wide exclusive scan of (lp, lw): warp scans, then the warp totals
     long long ip = lp, iw = lw;
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
       const SeqInfo s = load_seq(b, s_sl, s_qsl, p.max_pages, p.n_q_total);
       const int pages = scan_pages(p, s);
       rp += pages;
-      rw += pages * page_weight(s.n_q);
+      rw += seq_weight(pages, s.n_q);
     }
     if (tid == kScanThreads - 1) {
       s_prefix[p.n_seqs] = (int)rp;
@@ -221,6 +227,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
   const uint32_t tmem = *s_tmem;
 
   // CTA c scans the pages whose weighted cost falls in [c W / G, (c+1) W / G)
+  // (each sequence's segment cost placed before its pages)
   const long long w_total = s_wpre[p.n_seqs];
   auto page_at = [&](long long x) -> long long {
     if (x >= w_total) return s_prefix[p.n_seqs];
@@ -229,8 +236,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) indexer_scan_kernel(ScanParam
       const int mid = (lo + hi + 1) >> 1;
       if (s_wpre[mid] <= x) lo = mid; else hi = mid - 1;
     }
+    // the sequence's segment starts come first on the weighted axis
     const SeqInfo s = load_seq(lo, s_sl, s_qsl, p.max_pages, p.n_q_total);
-    return s_prefix[lo] + (x - s_wpre[lo]) / page_weight(s.n_q);
+    const long long seg = (long long)((s.n_q + kNqMax - 1) / kNqMax) * kSegmentCost;
+    return s_prefix[lo] + max(0ll, x - s_wpre[lo] - seg) / page_weight(s.n_q);
   };
   // one thread computes the range (64-bit divisions are slow in every thread)
   long long* s_range = reinterpret_cast<long long*>(smem + kOffMisc + 8);
