@@ -37,15 +37,20 @@ namespace msa {
 namespace {
 
 constexpr int kQkvThreads = 192;
-constexpr int kQkvStages = 2;
-constexpr int kHeadsPerCta = 2;               // N = 256
 constexpr int kChunk = 64;                    // bf16 elements of K per stage (128 bytes)
 constexpr int kTileBytes = 128 * kChunk * 2;  // 16 KB per 128-row operand tile
-constexpr int kOffA = 0;                                          // kQkvStages x 16 KB of x
-constexpr int kOffB = kQkvStages * kTileBytes;                    // kQkvStages x 32 KB of W (two heads)
-constexpr int kOffGamma = kOffB + kQkvStages * kHeadsPerCta * kTileBytes;  // 3 x 128 floats
-constexpr int kOffBarQ = kOffGamma + 3 * 128 * 4;
-constexpr int kQkvSmem = kOffBarQ + 8 * (2 * kQkvStages + 1) + 16;  // + tmem slot, abort, copies issued
+// Tile of H heads per CTA (N = 128 H): the widest N does the most work per
+// tcgen05.mma, one head per CTA makes twice the CTAs for short inputs.  The
+// ring is sized so that two CTAs fit per SM.
+template <int H>
+struct QkvTile {
+  static constexpr int kStages = H == 2 ? 2 : 3;
+  static constexpr int kOffA = 0;                                      // kStages x 16 KB of x
+  static constexpr int kOffB = kStages * kTileBytes;                   // kStages x H x 16 KB of W
+  static constexpr int kOffGamma = kOffB + kStages * H * kTileBytes;   // 3 x 128 floats
+  static constexpr int kOffBarQ = kOffGamma + 3 * 128 * 4;
+  static constexpr int kSmem = kOffBarQ + 8 * (2 * kStages + 1) + 16;  // + tmem slot, abort, copies issued
+};
 constexpr int kHeadsOut = kQHeads + 2 * kKvHeads + 1;  // 25
 
 struct QkvParams {
@@ -125,7 +130,11 @@ __device__ __forceinline__ void store_nvfp4_row(const float (&y)[128], float s_e
         make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
 }
 
+template <int kHeadsPerCta>
 __global__ void __launch_bounds__(kQkvThreads, 2) qkv_fused_kernel(const __grid_constant__ QkvParams p) {
+  using Tl = QkvTile<kHeadsPerCta>;
+  constexpr int kQkvStages = Tl::kStages;
+  constexpr int kOffA = Tl::kOffA, kOffB = Tl::kOffB, kOffGamma = Tl::kOffGamma, kOffBarQ = Tl::kOffBarQ;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -385,7 +394,11 @@ cudaError_t launch_qkv_fused(const msa_cache* c, const void* x, const void* w, i
   static DeviceSetup setup;
   int dev = 0, n_sm = 0;
   cudaError_t e = setup.get(&dev, &n_sm, [](int) {
-    return cudaFuncSetAttribute(qkv_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmem + 1024);
+    cudaError_t r = cudaFuncSetAttribute(qkv_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         QkvTile<1>::kSmem + 1024);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(qkv_fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                QkvTile<2>::kSmem + 1024);
   });
   if (e != cudaSuccess) return e;
   QkvParams qp{};
@@ -410,8 +423,15 @@ cudaError_t launch_qkv_fused(const msa_cache* c, const void* x, const void* w, i
   qp.y_out = y_out;
   qp.status = c->status;
   qp.wait_ns = launch_settings().wait_ns;
-  const dim3 grid((n_tokens + 127) / 128, (kHeadsOut + kHeadsPerCta - 1) / kHeadsPerCta);
-  qkv_fused_kernel<<<grid, kQkvThreads, kQkvSmem + 1024, stream>>>(qp);
+  // two heads per CTA once that still fills two full waves of two CTAs per SM
+  const int tiles = (n_tokens + 127) / 128;
+  if ((long long)tiles * ((kHeadsOut + 1) / 2) >= 4ll * n_sm) {
+    const dim3 grid(tiles, (kHeadsOut + 1) / 2);
+    qkv_fused_kernel<2><<<grid, kQkvThreads, QkvTile<2>::kSmem + 1024, stream>>>(qp);
+  } else {
+    const dim3 grid(tiles, kHeadsOut);
+    qkv_fused_kernel<1><<<grid, kQkvThreads, QkvTile<1>::kSmem + 1024, stream>>>(qp);
+  }
   return cudaGetLastError();
 }
 

@@ -107,3 +107,16 @@ def test_fused_projection_full_size_sampled():
     tokens = sorted(set([0, 1, 127, 128, 4095, 4096, n - 1] + [int(t) for t in rng.integers(0, n, 17)]))
     _check_rows(inp, table, y.cpu().numpy(), q8.cpu().numpy(), cache, tokens)
     assert cache.read_status() == 0
+
+
+def test_fused_projection_two_heads_per_cta_ragged_tail():
+    # 47 token tiles x 13 head pairs: the two-heads-per-CTA tile, with a last
+    # tile of 112 tokens (rows past the input read as zeros and are not stored)
+    n, d = 6000, 512
+    inp = workloads.qkv_inputs(n, d, seed=11, device=DEV)
+    cache, table, q8, y = _run(inp)
+    rng = np.random.default_rng(5)
+    tokens = sorted(set([0, 127, 128, 5887, 5888, 5950, n - 1] + [int(t) for t in rng.integers(0, n, 13)]))
+    _check_rows(inp, table, y.cpu().numpy(), q8.cpu().numpy(), cache, tokens)
+    assert cache.read_status() == 0
+
