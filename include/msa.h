@@ -406,11 +406,18 @@ int msa_debug_fp8_page(const msa_cache* cache, int64_t page, uint8_t* k8, uint8_
  *                               more than the launch has, so every CTA's wait
  *                               runs out after wait_limit_ns: the call sets
  *                               MSA_STATUS_TIMEOUT, leaves sel/n_sel unwritten
- *                               and its workspace barrier word at rest.
+ *                               and its workspace barrier word at rest;
+ *   MSA_INJECT_ATTENTION_TIMEOUT  every CTA of the attention kernel leaves out
+ *                               the copy of its first page, so the waits for it
+ *                               run out after wait_limit_ns: the call sets
+ *                               MSA_STATUS_TIMEOUT, its CTAs release tensor
+ *                               memory only after their copies and tensor-core
+ *                               products in flight are done, and return.
  * Launches already captured into a CUDA graph keep the settings they were
  * captured with.  Unknown flags return MSA_ERR_INVALID_ARG.
  */
 #define MSA_INJECT_BARRIER_TIMEOUT 0x1
+#define MSA_INJECT_ATTENTION_TIMEOUT 0x2
 int msa_debug_set_fault_injection(int32_t flags, uint64_t wait_limit_ns);
 
 /* Copies the device status word to *host_out (synchronous on the stream). */

@@ -119,6 +119,7 @@ struct AttnParams {
   float* lse_part;   // [T][S][16]
   int* status;
   unsigned long long wait_ns;  // limit of one bounded wait
+  int skip_first_copy;         // test hook: the producer leaves out page 0's copy (its waits run out)
 };
 
 // OR of a predicate over the threads of a named barrier (all of them wait).
@@ -290,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         for (int i = 0; i < n; ++i, ++e) {
           const int st = e % kStages;
           if (!mbar_wait(bar(kRawEmpty + st), ((e / kStages) & 1) ^ 1, wc)) { ok = false; break; }
+          if (e == 0 && p.skip_first_copy) continue;  // nothing will complete stage 0
           mbar_arrive_expect_tx(bar(kRawFull + st), kHeadBytes);
           bulk_g2s(sbase + kOffRaw + st * kHeadBytes, head + (size_t)r->phys[i] * kKvPageBytes, kHeadBytes,
                    bar(kRawFull + st));
@@ -642,7 +644,8 @@ cudaError_t launch_sparse_attn_tc(const msa_cache* c, const uint8_t* q, float so
   AttnParams ap{static_cast<const uint8_t*>(c->kv_pool), c->n_pages, q, sel, n_sel, block_table,
                 max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, n_splits, n_items,
                 softmax_scale / c->s_enc_k * kLog2e, 1.0f / c->s_enc_v, o_part,
-                lse_part, c->status, launch_settings().wait_ns};
+                lse_part, c->status, launch_settings().wait_ns,
+                (launch_settings().inject & kInjectAttentionTimeout) ? 1 : 0};
   const int grid = n_items < n_sm ? n_items : n_sm;
   return launch_pdl(sparse_attn_tc_kernel, dim3(grid), dim3(kThreads), attn_smem_bytes(n_seqs), stream, ap);
 }

@@ -324,7 +324,7 @@ int msa_unpack_blocks(const msa_cache* layers, int32_t n_layers, const uint8_t* 
 }
 
 int msa_debug_set_fault_injection(int32_t flags, uint64_t wait_limit_ns) {
-  if (flags & ~MSA_INJECT_BARRIER_TIMEOUT) return MSA_ERR_INVALID_ARG;
+  if (flags & ~(MSA_INJECT_BARRIER_TIMEOUT | MSA_INJECT_ATTENTION_TIMEOUT)) return MSA_ERR_INVALID_ARG;
   msa::g_wait_ns.store(wait_limit_ns ? (unsigned long long)wait_limit_ns : msa::kDefaultWaitLimitNs,
                        std::memory_order_relaxed);
   msa::g_inject.store(flags, std::memory_order_relaxed);

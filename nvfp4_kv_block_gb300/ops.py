@@ -28,6 +28,7 @@ TOPK = 16
 KV_PAGE_BYTES = 73_728
 NOALLOC_SCRATCH_BYTES = 8 << 20  # MSA_INDEXER_NOALLOC_SCRATCH_BYTES
 INJECT_BARRIER_TIMEOUT = 0x1     # MSA_INJECT_BARRIER_TIMEOUT
+INJECT_ATTENTION_TIMEOUT = 0x2   # MSA_INJECT_ATTENTION_TIMEOUT
 STATUS_BAD_SLOT, STATUS_BAD_PAGE, STATUS_BAD_SEQ, STATUS_BAD_SELECTION, STATUS_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
 IDX_PAGE_BYTES = 16_384
 
@@ -370,7 +371,8 @@ def qkv_project_insert(cache, x, w, gamma_q, gamma_k, gamma_idx, cos_sin, positi
 
 def set_fault_injection(flags=0, wait_limit_ns=0):
     """Test hook: wait limit of every later launch (0 = the 2 s default) and
-    fault-injection flags (INJECT_BARRIER_TIMEOUT); 0, 0 restores the defaults."""
+    fault-injection flags (INJECT_BARRIER_TIMEOUT, INJECT_ATTENTION_TIMEOUT); 0, 0 restores
+    the defaults."""
     _check(lib().msa_debug_set_fault_injection(int(flags), int(wait_limit_ns)))
 
 

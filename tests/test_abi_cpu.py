@@ -100,6 +100,9 @@ def test_block_rows_validation_needs_no_gpu(lib):
 def test_fault_injection_settings_are_validated_on_the_host(lib):
     assert lib.msa_debug_set_fault_injection(0x100, 0) == -1
     assert lib.msa_debug_set_fault_injection(ops.INJECT_BARRIER_TIMEOUT, 1000) == 0
+    assert lib.msa_debug_set_fault_injection(ops.INJECT_ATTENTION_TIMEOUT, 1000) == 0
+    assert lib.msa_debug_set_fault_injection(ops.INJECT_BARRIER_TIMEOUT | ops.INJECT_ATTENTION_TIMEOUT, 1000) == 0
+    assert lib.msa_debug_set_fault_injection(0x4, 0) == -1
     assert lib.msa_debug_set_fault_injection(0, 0) == 0
 
 

@@ -1,12 +1,14 @@
 """Failure detection without a GPU fault: a bounded wait that runs out.
 
-A test hook of the library makes the indexer's grid barrier wait for one CTA
-more than the launch has, with a wait limit of a few milliseconds.  Every CTA's
-wait then runs out; the call reports MSA_STATUS_TIMEOUT without touching its
+Test hooks of the library (a few-millisecond wait limit): the indexer's grid
+barrier waits for one CTA more than the launch has; the attention kernel's
+producer leaves out its first copy.  The indexer's CTAs all run out of
+time at the barrier; the call reports MSA_STATUS_TIMEOUT without touching its
 outputs, and the barrier word is back at rest, so the next normal call on the
 same workspace, and on the allocation-free entry point's static scratch,
-selects exactly as before.  Nothing here faults, traps or hangs: each wait
-ends after its limit.
+selects exactly as before.  The attention's CTAs run out of time waiting for
+the missing page, report MSA_STATUS_TIMEOUT and return; the next call is exact.
+Nothing here faults, traps or hangs: each wait ends after its limit.
 """
 
 import numpy as np
@@ -62,3 +64,32 @@ def test_barrier_timeout_is_reported_and_the_next_calls_recover():
     assert st.cache.read_status() == 0
     word = int(ws[:8].view(torch.int64).item())
     assert word & 0xFFFFFFFF == 0 and (word >> 32) >= 3  # three completed barriers
+
+
+def test_attention_timeout_is_reported_and_the_next_call_recovers():
+    # every attention CTA leaves out the copy of its first page: the waits for
+    # it run out, every role of the CTA gives up, the CTA waits (bounded) for
+    # its copies and tensor-core products in flight, frees tensor memory and
+    # returns; the next call on the same cache is exact again
+    wl = workloads.custom("attn_timeout", [4096, 2000, 9000], [1, 2, 3], seed=9, permuted=True)
+    st = harness.build_state(wl, DEV)
+    q, qi, w = wl.queries(DEV)
+    sel, n_sel, _ = ops.indexer_topk(st.cache, qi, w, st.block_table, st.seq_lens, st.q_start_loc)
+    args = (st.cache, q, sel, n_sel, st.block_table, st.seq_lens, st.q_start_loc, 1)
+    ref_o, ref_l = ops.sparse_attn_decode(*args)
+    torch.cuda.synchronize()
+    ref_o, ref_l = ref_o.clone(), ref_l.clone()
+    assert st.cache.read_status() == 0
+    try:
+        ops.set_fault_injection(ops.INJECT_ATTENTION_TIMEOUT, LIMIT_NS)
+        ops.sparse_attn_decode(*args)
+        torch.cuda.synchronize()
+        assert st.cache.read_status() == ops.STATUS_TIMEOUT
+    finally:
+        ops.set_fault_injection(0, 0)
+    st.cache.status.zero_()
+    for _ in range(2):
+        o, l = ops.sparse_attn_decode(*args)
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
+    assert st.cache.read_status() == 0
