@@ -43,6 +43,7 @@
 namespace msa {
 namespace {
 
+constexpr int kInjectAttentionTimeout = 2;  // test hook: the producer leaves out its first copy
 constexpr int kGroups = 2;     // conversion warpgroups
 constexpr int kWarpConv0 = 8;  // warps 0-3 roles, 4-7 softmax
 constexpr int kThreads = 32 * (kWarpConv0 + 4 * kGroups);

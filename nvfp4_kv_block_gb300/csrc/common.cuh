@@ -513,8 +513,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // ---- host-side launch settings ----------------------------------------------------
 // Library-wide settings every launch reads (msa_debug_set_fault_injection):
 // the limit of one bounded wait, and test-only fault-injection flags.
-constexpr int kInjectBarrierTimeout = 1;    // the indexer's grid barrier waits for one CTA more than exist
-constexpr int kInjectAttentionTimeout = 2;  // the attention's producer leaves out its first copy
+constexpr int kInjectBarrierTimeout = 1;  // the indexer's grid barrier waits for one CTA more than exist
 struct LaunchSettings {
   unsigned long long wait_ns;
   int inject;
