@@ -13,27 +13,31 @@
 // takes items c, c + G, c + 2G, ...; its pages (numbered e = 0, 1, ... across
 // its items) flow through warp roles, every hand-off an mbarrier and every
 // wait bounded:
-//   warp 0       scheduler: per item, the sequence of j (shared-memory copy of
-//                q_start_loc), the selected blocks, their physical pages and the
-//                tokens visible in each, and the 4 query rows as a swizzled
-//                tile, into a 4-deep ring of item records;
-//   warp 1       TMA producer: one 18,432-byte cp.async.bulk copy per page (the
-//                KV head's K and V codes and scales) into a ring of stages;
-//   warp 2       QK issuer: S = K8 Q^T (kind::f8f6f4, M = 128 tokens, N = 16: the
-//                4 query heads, zero padded, K = 128, A from tensor memory);
-//   warp 3       PV issuer: O^T += V8^T P (A = the V tile read MN-major, no
-//                transpose, B = P), accumulated in tensor memory over the
-//                item's pages (one buffer per item parity); its commit per page
-//                frees the page's V tile and P tile;
-//   warps 4-7    softmax, thread = token row of S: P = 256 * 2^(x - m) for a
+//   warp 0       scheduler and TMA producer: per item, the sequence of j
+//                (a 32-way search of q_start_loc, copied to shared memory when
+//                it fits beside the rings), the selected blocks, their
+//                physical pages and the tokens visible in each, and the 4 query
+//                rows as a swizzled tile, into a ring of kRecs item records;
+//                then one 18,432-byte cp.async.bulk copy per page of the item
+//                (the KV head's K and V codes and scales) into a ring of stages;
+//   warps 1-2    QK issuers, warp 1 + s for the pages of set s (e % 2 == s):
+//                S = K8 Q^T (kind::f8f6f4, M = 128 tokens, N = 16: the 4 query
+//                heads, zero padded, K = 128, A from tensor memory);
+//   warps 3-4    PV issuers, warp 3 + s for set s: O_s^T += V8^T P (A = the V
+//                tile read MN-major, no transpose, B = P), accumulated in tensor
+//                memory over the item's pages, one buffer per set and item
+//                parity; the commit per page frees the page's V tile and P tile;
+//   warps 5-12   softmax, two sets of 4 warps; set s takes the pages with
+//                e % 2 == s, thread = token row of S: P = 256 * 2^(x - m) for a
 //                reference m per head that changes only when a row of the page
 //                exceeds it by more than kGrowth (then m = page max + kHeadroom,
-//                the running row sums and the O accumulator are rescaled);
-//                P is written as two E4M3 terms (value + rounding remainder),
-//                the B operand of PV.  At the item's end, thread = channel: the
-//                normalised partial (O, LSE); the LSE merge kernel combines
-//                the splits;
-//   warps 8 ..   kGroups conversion warpgroups; group g converts the pages with
+//                and the set's row sums and O accumulator are rescaled); P is
+//                written as two E4M3 terms (value + rounding remainder), the B
+//                operand of PV.  At the item's end set 1 hands its (m, row sum)
+//                to set 0, which reads both O accumulators (thread = channel)
+//                and writes the normalised partial (O, LSE); the LSE merge
+//                kernel combines the splits;
+//   warps 13 ..  kGroups conversion warpgroups; group g converts the pages with
 //                e % kGroups == g, thread = token: NVFP4 -> FP8 through a
 //                256-entry shared table of scaled E4M3 values and byte
 //                permutes, K written with tcgen05.st straight into tensor memory
@@ -44,12 +48,14 @@ namespace msa {
 namespace {
 
 constexpr int kInjectAttentionTimeout = 2;  // test hook: the producer leaves out its first copy
-constexpr int kGroups = 2;     // conversion warpgroups
-constexpr int kWarpConv0 = 8;  // warps 0-3 roles, 4-7 softmax
+constexpr int kGroups = 3;      // conversion warpgroups
+constexpr int kSets = 2;        // softmax sets (set = e % 2, also the S slot)
+constexpr int kWarpSmax0 = 1 + 2 * kSets;  // warp 0 scheduler and producer, then a QK and a PV issuer per set
+constexpr int kWarpConv0 = kWarpSmax0 + 4 * kSets;
 constexpr int kThreads = 32 * (kWarpConv0 + 4 * kGroups);
 constexpr int kStages = 6;     // raw page ring
-constexpr int kRecs = 4;       // item records in flight
-constexpr int kSlots = 4;      // K8 buffers (tensor memory), V8 tiles and P tiles: slot = e % kSlots
+constexpr int kRecs = 3;       // item records in flight
+constexpr int kSlots = 6;      // K8 buffers (tensor memory), V8 tiles and P tiles: slot = e % kSlots
 // A group waits only for its own pages' slots and stages; for a parity wait
 // never to see a phase two behind, the same group must own every page of a
 // slot (and of a stage): kGroups divides both ring sizes.
@@ -61,23 +67,26 @@ constexpr int kOffP = kOffQ + kRecs * 2048;            // kSlots x [128 tokens][
 constexpr int kOffRaw = kOffP + kSlots * 2048;         // kStages x 18,432
 constexpr int kOffTab = kOffRaw + kStages * kHeadBytes;  // uint2 [256]
 constexpr int kOffRec = kOffTab + 2048;                // kRecs x 256 B
-constexpr int kOffRed = kOffRec + kRecs * 256;         // float [4 warps][4 heads] page maxima
-constexpr int kOffRedL = kOffRed + 64;                 // float [4 warps][4 heads] row sums
-constexpr int kOffBars = kOffRedL + 64;
+constexpr int kOffRed = kOffRec + kRecs * 256;         // float [set][4 warps][4 heads] page maxima
+constexpr int kOffRedL = kOffRed + 64 * kSets;         // float [set][4 warps][4 heads] row sums
+constexpr int kOffMerge = kOffRedL + 64 * kSets;       // float [item parity][m 4, L 4] of set 1
+constexpr int kOffBars = kOffMerge + 64;
 // barrier indices
 constexpr int kRawFull = 0, kRawEmpty = kStages, kK8Full = 2 * kStages, kK8Empty = kK8Full + kSlots,
               kSFull = kK8Empty + kSlots, kSEmpty = kSFull + 2, kV8Full = kSEmpty + 2,
               kPFull = kV8Full + kSlots, kPVDone = kPFull + kSlots, kOFree = kPVDone + kSlots,
-              kRecFull = kOFree + 2, kRecEmpty = kRecFull + kRecs, kDone = kRecEmpty + kRecs,
-              kNumBars = kDone + 2;  // kDone: QK issuer, kDone + 1: PV issuer
+              kMergeFull = kOFree + 2, kMergeEmpty = kMergeFull + 2,
+              kRecFull = kMergeEmpty + 2, kRecEmpty = kRecFull + kRecs, kDone = kRecEmpty + kRecs,
+              kNumBars = kDone + 1;  // kDone: every MMA of the CTA is done (one commit per issuer)
 constexpr int kOffMisc = kOffBars + ((kNumBars * 8 + 15) / 16) * 16;  // tmem, abort, issued pages
 constexpr int kOffQsl = kOffMisc + 16;  // int [n_seqs + 1] copy of q_start_loc
 constexpr uint32_t kTmS = 32 * kSlots;  // TMEM columns: K8 slot i at 32 i, S slot s at kTmS + 16 s,
-constexpr uint32_t kTmO = kTmS + 32;    // O buffer b at kTmO + 16 b
-constexpr uint32_t kTmemCols = 256;
-static_assert(kTmO + 32 <= kTmemCols, "tensor memory columns");
-// producer, QK issuer (a commit), PV issuer, 4 softmax warps, the conversion warps
-constexpr int kRecEmptyCount = 3 + 4 + 4 * kGroups;
+constexpr uint32_t kTmO = kTmS + 32;    // O of set s for item parity b at kTmO + 16 (2 b + s)
+constexpr uint32_t kTmemCols = 512;
+static_assert(kTmO + 64 <= kTmemCols, "tensor memory columns");
+static_assert(kSets == 2, "S slots, O buffers and the merge are laid out for two sets");
+// producer, QK issuers (a commit: the Q tile), PV issuers, the softmax warps, the conversion warps
+constexpr int kRecEmptyCount = 1 + 2 * kSets + 4 * kSets + 4 * kGroups;
 // P = 256 * 2^(x - m) must stay below the largest finite E4M3 value (448):
 // a row more than kGrowth above m (256 * 2^0.75 = 430.5) moves m to the page
 // max + kHeadroom, so that later pages rarely move it again.
@@ -89,7 +98,11 @@ static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1 KB 
 static_assert(kOffRaw % 16 == 0 && kHeadBytes % 16 == 0, "bulk copy alignment");
 static_assert(kOffVs - kOffVc == kOffKs - kOffKc, "K and V halves share one layout");
 
-size_t attn_smem_bytes(int n_seqs) { return 1024 + kOffQsl + 4 * (size_t)(n_seqs + 1); }
+constexpr int kSmemOptin = 232448;  // largest dynamic shared memory of one CTA (227 KB)
+constexpr int kQslShared = (kSmemOptin - 1024 - kOffQsl) / 4;  // q_start_loc entries that fit beside the rings
+static_assert(kQslShared >= 2, "shared memory");
+bool qsl_fits(int n_seqs) { return n_seqs + 1 <= kQslShared; }
+size_t attn_smem_bytes(int n_seqs) { return 1024 + kOffQsl + (qsl_fits(n_seqs) ? 4 * (size_t)(n_seqs + 1) : 0); }
 
 // One item record (256 bytes of shared memory).
 struct ItemRec {
@@ -120,8 +133,18 @@ struct AttnParams {
   float* lse_part;   // [T][S][16]
   int* status;
   unsigned long long wait_ns;  // limit of one bounded wait
+  int qsl_shared;              // q_start_loc copied to shared memory (else read from global)
   int skip_first_copy;         // test hook: the producer leaves out page 0's copy (its waits run out)
 };
+
+// 16 registers per thread -> 32 TMEM lanes x 16 columns (thread = lane).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 
 // OR of a predicate over the threads of a named barrier (all of them wait).
 __device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred) {
@@ -188,14 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSFull + i), 1);
       mbar_init(bar(kSEmpty + i), 4);
-      mbar_init(bar(kOFree + i), 4);
+      mbar_init(bar(kOFree + i), 4);       // set 0 has read both O buffers of this parity
+      mbar_init(bar(kMergeFull + i), 4);   // set 1's (m, L) written
+      mbar_init(bar(kMergeEmpty + i), 4);  // set 0 has read them
     }
     for (int i = 0; i < kRecs; ++i) {
       mbar_init(bar(kRecFull + i), 1);
       mbar_init(bar(kRecEmpty + i), kRecEmptyCount);
     }
-    mbar_init(bar(kDone), 1);
-    mbar_init(bar(kDone + 1), 1);
+    mbar_init(bar(kDone), 2 * kSets);
     *s_abort = 0;
     *s_issued = 0;
     fence_barrier_init();
@@ -204,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   for (int i = tid; i < (kRecs + kSlots) * 2048 / 16; i += kThreads)
     reinterpret_cast<uint4*>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
   // q_start_loc does not come from the previous kernel
-  for (int i = tid; i <= p.n_seqs; i += kThreads) s_qsl[i] = p.q_start_loc[i];
+  if (p.qsl_shared)
+    for (int i = tid; i <= p.n_seqs; i += kThreads) s_qsl[i] = p.q_start_loc[i];
   if (warp == 2) tmem_alloc(smem_u32(s_tmem), kTmemCols);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -215,18 +240,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   pdl_trigger();
 
   if (warp == 0) {
-    // ---------------- scheduler: item records ------------------------------------------
-    for (int k = 0; k < n_mine; ++k) {
+    // ---------------- scheduler and TMA producer ---------------------------------------------
+    // per item: the record (all lanes), then lane 0 streams the item's pages
+    const int* qsl = p.qsl_shared ? s_qsl : p.q_start_loc;
+    int e = 0;
+    bool ok = true;
+    for (int k = 0; ok && k < n_mine; ++k) {
       const int slot = k % kRecs;
       if (!warp_wait(bar(kRecEmpty + slot), ((k / kRecs) & 1) ^ 1, wc)) break;
       const int item = blockIdx.x + k * G;
       const int split = item % p.n_splits, kvh = (item / p.n_splits) % kKvHeads;
       const int j = item / (p.n_splits * kKvHeads);
-      // sequence b of token j: the last b with q_start_loc[b] <= j (binary search)
-      int lo = 0, hi = p.n_seqs - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_qsl[mid] <= j) lo = mid; else hi = mid - 1;
+      // sequence b of token j: the last b with q_start_loc[b] <= j.  32-ary
+      // search, each round one sample per lane over the remaining range; a
+      // malformed q_start_loc still gives an index in range, rejected below
+      int lo = 0, span = p.n_seqs;
+      while (span > 1) {
+        const int step = (span + 31) >> 5, idx = lo + lane * step;
+        const bool le = idx < lo + span && qsl[idx] <= j;
+        const int cnt = max(__popc(__ballot_sync(0xffffffffu, le)), 1);
+        const int nlo = lo + (cnt - 1) * step;
+        span = min(step, lo + span - nlo);
+        lo = nlo;
       }
       const int b = p.n_seqs > 0 ? lo : -1;
       // first round of loads, all independent: sequence length, selection, query rows
@@ -236,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       const int blk_raw = lane < kSelStride && e_sel < kSelStride ? p.sel[(size_t)j * kSelStride + e_sel] : -1;
       const uint4 qv = *reinterpret_cast<const uint4*>(
           p.q + ((size_t)j * kQHeads + kvh * kGqa + (lane >> 3)) * kHeadDim + 16 * (lane & 7));
-      const int q0 = b >= 0 ? s_qsl[b] : 0, n_q = b >= 0 ? s_qsl[b + 1] - q0 : 0;
+      const int q0 = b >= 0 ? qsl[b] : 0, n_q = b >= 0 ? qsl[b + 1] - q0 : 0;
       const bool seq_ok = b >= 0 && q0 <= j && j < q0 + n_q && q0 >= 0 && q0 + n_q <= p.n_q_total &&
                           seq_len >= n_q && seq_len <= p.max_pages * kPageTokens;
       const int pos = seq_len - n_q + (j - q0);
@@ -263,8 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         r->phys[at] = phys;
         r->valid[at] = blk_raw == r_blk ? (pos % kPageTokens) + 1 : kPageTokens;
       }
+      const int n = __popc(okmask);
       if (lane == 0) {
-        r->n_pg = __popc(okmask);
+        r->n_pg = n;
         r->j = j;
         r->kvh = kvh;
         r->split = split;
@@ -276,19 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kRecFull + slot));
-    }
-  } else if (warp == 1) {
-    // ---------------- TMA producer: one copy per page (K and V halves) -----------------
-    if (lane == 0) {
-      int e = 0;
-      bool ok = true;
-      for (int k = 0; ok && k < n_mine; ++k) {
-        const int slot = k % kRecs;
-        if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc)) break;
-        const ItemRec* r = rec(slot);
-        const int n = r->n_pg;
-        const uint8_t* head = p.kv_pool + (size_t)r->kvh * kHeadBytes;
+      if (lane == 0) {
+        mbar_arrive(bar(kRecFull + slot));
+        // one copy per page: the KV head's K and V codes and scales
+        const uint8_t* head = p.kv_pool + (size_t)kvh * kHeadBytes;
         for (int i = 0; i < n; ++i, ++e) {
           const int st = e % kStages;
           if (!mbar_wait(bar(kRawEmpty + st), ((e / kStages) & 1) ^ 1, wc)) { ok = false; break; }
@@ -300,57 +327,61 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         }
         if (ok) mbar_arrive(bar(kRecEmpty + slot));
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ---------------- QK issuer ---------------------------------------------------------------
+  } else if (warp < 1 + kSets) {
+    // ---------------- QK issuers: warp 1 + s takes the pages of set s (e % 2 == s) ---------------
     if (lane == 0) {
+      const int s = warp - 1;
       const uint32_t idesc = umma_idesc_e4m3(128, 16);
-      int e = 0;
+      int e0 = 0;
       bool ok = true;
       for (int k = 0; ok && k < n_mine; ++k) {
         const int slot = k % kRecs;
         if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc)) break;
         const int n = rec(slot)->n_pg;
         const uint64_t bdesc = umma_desc_sw128(sbase + kOffQ + slot * 2048);
-        for (int i = 0; i < n; ++i, ++e) {
-          const int ks = e % kSlots, kph = (e / kSlots) & 1, sl = e & 1, sph = (e >> 1) & 1;
-          if (!mbar_wait(bar(kK8Full + ks), kph, wc) || !mbar_wait(bar(kSEmpty + sl), sph ^ 1, wc)) {
+        bool issued = false;
+        for (int i = (s - e0) & 1; i < n; i += kSets) {
+          const int e = e0 + i, ks = e % kSlots, kph = (e / kSlots) & 1, sph = (e >> 1) & 1;
+          if (!mbar_wait(bar(kK8Full + ks), kph, wc) || !mbar_wait(bar(kSEmpty + s), sph ^ 1, wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // K = 32 per MMA: 8 TMEM columns of A, +32 B (+2) of B
-            umma_e4m3_ts(tmem + kTmS + 16 * sl, tmem + 32 * ks + 8 * kk, bdesc + 2 * kk, idesc, kk > 0);
+            umma_e4m3_ts(tmem + kTmS + 16 * s, tmem + 32 * ks + 8 * kk, bdesc + 2 * kk, idesc, kk > 0);
           umma_commit(bar(kK8Empty + ks));
-          umma_commit(bar(kSFull + sl));
+          umma_commit(bar(kSFull + s));
+          issued = true;
         }
         if (!ok) break;
         // the record's Q tile is free once these MMAs are done
-        if (n > 0) umma_commit(bar(kRecEmpty + slot));
+        if (issued) umma_commit(bar(kRecEmpty + slot));
         else mbar_arrive(bar(kRecEmpty + slot));
+        e0 += n;
       }
       umma_commit(bar(kDone));  // arrives when every MMA of this thread is done
     }
     __syncwarp();
-  } else if (warp == 3) {
-    // ---------------- PV issuer ---------------------------------------------------------------
+  } else if (warp < 1 + 2 * kSets) {
+    // ---------------- PV issuers: warp 1 + kSets + s takes the pages of set s -------------------
     if (lane == 0) {
+      const int s = warp - 1 - kSets;
       const uint32_t idesc = umma_idesc_e4m3_amn_bmn(128, 16);
-      int e = 0, ni = 0;  // ni: items with pages so far (O buffer ni & 1)
+      int e0 = 0, ni = 0;  // ni: items with pages so far (O buffer parity ni & 1)
       bool ok = true;
       for (int k = 0; ok && k < n_mine; ++k) {
         const int slot = k % kRecs;
         if (!mbar_wait(bar(kRecFull + slot), (k / kRecs) & 1, wc)) break;
         const int n = rec(slot)->n_pg;
         mbar_arrive(bar(kRecEmpty + slot));  // nothing else of the record is needed
-        if (n == 0) continue;
-        const int ob = ni & 1;
-        // O buffer ob is free once the softmax has read item ni - 2's output from it
-        if (ni >= 2 && !mbar_wait(bar(kOFree + ob), ((ni >> 1) - 1) & 1, wc)) break;
-        for (int i = 0; i < n; ++i, ++e) {
-          const int v = e % kSlots, vph = (e / kSlots) & 1;
+        const int ob = ni & 1, i0 = (s - e0) & 1;
+        // O buffers of parity ob are free once set 0 has read item ni - 2's output from them
+        if (n > i0 && ni >= 2 && !mbar_wait(bar(kOFree + ob), ((ni >> 1) - 1) & 1, wc)) break;
+        for (int i = i0; i < n; i += kSets) {
+          const int e = e0 + i, v = e % kSlots, vph = (e / kSlots) & 1;
           if (!mbar_wait(bar(kV8Full + v), vph, wc) || !mbar_wait(bar(kPFull + v), vph, wc)) {
             ok = false;
             break;
@@ -365,14 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
             const uint64_t adesc =
                 umma_desc_sw128_lbo_sbo(sbase + kOffV8 + v * kTileBytes + kk * 4096, 1024, 1024);
             const uint64_t bdesc = umma_desc_noswz_lbo_sbo(sbase + kOffP + v * 2048 + kk * 512, 128, 128);
-            umma_e4m3(tmem + kTmO + 16 * ob, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            // set s's accumulator; its first page of the item (i < 2) overwrites it
+            umma_e4m3(tmem + kTmO + 16 * (2 * ob + s), adesc, bdesc, idesc, (i >= 2 || kk > 0) ? 1u : 0u);
           }
           // page e's V tile and P tile are free (and O holds page e) once this is done
           umma_commit(bar(kPVDone + v));
         }
-        ++ni;
+        if (n > 0) ++ni;
+        e0 += n;
       }
-      umma_commit(bar(kDone + 1));
+      umma_commit(bar(kDone));
     }
     __syncwarp();
   } else if (warp >= kWarpConv0) {
@@ -410,12 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
           break;
         }
         const uint8_t* raw = smem + kOffRaw + st * kHeadBytes;
-        uint32_t o[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) convert_chunk(raw + kOffKc + code_off[c], raw + kOffKc + sc_off[c], s_tab, o + 8 * c);
         // K: row tok of A in TMEM, columns 32 sl + 8c .. + 7 = channels 32c .. 32c + 31
         // (rows past the query position stay as converted: the softmax masks them)
-        tmem_st32(trow + 32 * sl, o);
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          uint32_t o[16];
+          convert_chunk(raw + kOffKc + code_off[2 * hc], raw + kOffKc + sc_off[2 * hc], s_tab, o);
+          convert_chunk(raw + kOffKc + code_off[2 * hc + 1], raw + kOffKc + sc_off[2 * hc + 1], s_tab, o + 8);
+          tmem_st16(trow + 32 * sl + 16 * hc, o);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -432,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         uint8_t* dst = smem + kOffV8 + sl * kTileBytes;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t* oc = o + 8 * c;
+          uint32_t oc[8];
           convert_chunk(raw + kOffVc + code_off[c], raw + kOffVc + sc_off[c], s_tab, oc);
           if (!full) {
 #pragma unroll
@@ -450,15 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       }
       if (ok && lane == 0) mbar_arrive(bar(kRecEmpty + slot));
     }
-  } else if (warp >= 4) {
-    // ---------------- softmax: warps 4-7 -------------------------------------------------------
-    // warp w reads TMEM lanes 32 (w % 4) ..: row = token of S, channel of O
-    const int quad = warp & 3, row = 32 * quad + lane;
+  } else if (warp >= kWarpSmax0) {
+    // ---------------- softmax: set s = warps 4 + 4 s .. 7 + 4 s --------------------------------
+    // set s takes the pages with e % 2 == s (S slot s); warp w reads TMEM lanes
+    // 32 (w % 4) ..: row = token of S, channel of O
+    const int set = (warp - kWarpSmax0) >> 2, quad = warp & 3, row = 32 * quad + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
-    constexpr int nb = 1;  // named barrier of the four warps
-    float* red = reinterpret_cast<float*>(smem + kOffRed);    // [4 warps][4 heads]
-    float* redl = reinterpret_cast<float*>(smem + kOffRedL);  // [4 warps][4 heads]
-    int e = 0, ni = 0;
+    const int nb = 1 + set;  // named barrier of the set's four warps
+    float* red = reinterpret_cast<float*>(smem + kOffRed) + 16 * set;    // [4 warps][4 heads]
+    float* redl = reinterpret_cast<float*>(smem + kOffRedL) + 16 * set;  // [4 warps][4 heads]
+    int e0 = 0, ni = 0;  // the item's first page; items with pages so far
     bool ok = true;
     for (int k = 0; ok && k < n_mine; ++k) {
       const int slot = k % kRecs;
@@ -466,22 +503,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       const ItemRec* r = rec(slot);
       const int n = r->n_pg;
       const int ob = ni & 1;
+      const uint32_t t_o = trow + kTmO + 16 * (2 * ob + set);  // this set's O accumulator
+      const int i0 = (set - e0) & 1;  // the set's first page of the item
       float m_ref[4], l_run[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         m_ref[h] = -INFINITY;
         l_run[h] = 0.f;
       }
-      for (int i = 0; i < n; ++i, ++e) {
-        const int sl = e & 1;
-        bool good = warp_wait(bar(kSFull + sl), (e >> 1) & 1, wc);
+      for (int i = i0; i < n; i += kSets) {
+        const int e = e0 + i;
+        bool good = warp_wait(bar(kSFull + set), (e >> 1) & 1, wc);
         float sv[4] = {0.f, 0.f, 0.f, 0.f};
         if (good) {
           tc_fence_after();
-          tmem_ld4(trow + kTmS + 16 * sl, sv);
+          tmem_ld4(trow + kTmS + 16 * set, sv);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kSEmpty + sl));
+          if (lane == 0) mbar_arrive(bar(kSEmpty + set));
         }
         const bool live = row < r->valid[i];
         float x[4];
@@ -492,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
           over = over || x[h] > m_ref[h] + kGrowth;
         }
         bool step_ok = true;
-        // a row above the reference (always on the item's first page), or an abort
+        // a row above the reference (always on the set's first page), or an abort
         if (named_barrier_or(nb, 128, over || !good || !ok)) {
           if (named_barrier_or(nb, 128, !good || !ok)) {
             ok = false;
@@ -517,22 +556,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
             l_run[h] *= f[h];
             m_ref[h] = m_new;
           }
-          if (i > 0) {
-            // O holds the item's earlier pages relative to the old reference:
-            // once their PVs are done (PV of page e - 1), rescale it in place
-            const int pv = (e - 1) % kSlots;
-            step_ok = warp_wait(bar(kPVDone + pv), ((e - 1) / kSlots) & 1, wc);
+          if (i >= kSets) {
+            // O holds the set's earlier pages of the item relative to the old
+            // reference: once their PVs are done (PV of page e - 2), rescale it
+            const int pv = (e - kSets) % kSlots;
+            step_ok = warp_wait(bar(kPVDone + pv), ((e - kSets) / kSlots) & 1, wc);
             if (step_ok) {
               tc_fence_after();
               float ov[8];
-              tmem_ld8(trow + kTmO + 16 * ob, ov);  // thread = channel: hi terms, then remainders
+              tmem_ld8(t_o, ov);  // thread = channel: hi terms, then remainders
               uint32_t ou[8];
 #pragma unroll
               for (int h = 0; h < 4; ++h) {
                 ou[h] = __float_as_uint(ov[h] * f[h]);
                 ou[4 + h] = __float_as_uint(ov[4 + h] * f[h]);
               }
-              tmem_st8(trow + kTmO + 16 * ob, ou);
+              tmem_st8(t_o, ou);
               tmem_wait_st();
               tc_fence_before();
             }
@@ -552,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         const uint32_t lo23 = cvt_e4m3x2_f16x2(hsub2_u32(cvt_f16x2_f32(v[3], v[2]), cvt_f16x2_e4m3x2(hi23)));
         // P tile row = token: bytes 0-3 hi terms of heads 0-3, 4-7 the remainders
         // (bytes 8-15 stay zero: they pad N to 16); tile e % kSlots is free once
-        // PV of page e - kSlots is done
+        // PV of page e - kSlots (this set's) is done
         const int po = e % kSlots;
         if (step_ok && e >= kSlots) step_ok = warp_wait(bar(kPVDone + po), ((e / kSlots) & 1) ^ 1, wc);
         if (step_ok) {
@@ -564,21 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         }
         ok = ok && step_ok;  // a failure here ends the loop at the next barrier
       }
-      // ---- the item's output: O after its last PV, thread = channel ---------------------------
-      float ov[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (ok && n > 0) {
-        const int pv = (e - 1) % kSlots;
-        ok = warp_wait(bar(kPVDone + pv), ((e - 1) / kSlots) & 1, wc);
-        if (ok) {
-          tc_fence_after();
-          tmem_ld8(trow + kTmO + 16 * ob, ov);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kOFree + ob));  // PV of item ni + 2 may overwrite it
-        }
-      }
       const bool aborted = named_barrier_or(nb, 128, !ok || *s_abort != 0);
-      // sum of p over the 128 rows, per head
+      // ---- this set's sum of p over the 128 rows, per head ----------------------------------------
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         float l = l_run[h];
@@ -587,18 +613,75 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
         if (lane == 0) redl[quad * 4 + h] = l;
       }
       named_barrier_sync(nb, 128);
-      const size_t row0 = ((size_t)r->j * p.n_splits + r->split) * kQHeads + r->kvh * kGqa;
+      float L[4];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float L = aborted ? 0.f : redl[h] + redl[4 + h] + redl[8 + h] + redl[12 + h];
-        const bool nonempty = !aborted && n > 0 && L > 0.f;
-        p.o_part[(row0 + h) * kHeadDim + row] = nonempty ? (ov[h] + ov[4 + h]) / L * p.out_scale : 0.f;
-        if (row == 0) p.lse_part[row0 + h] = nonempty ? (m_ref[h] + log2f(L) - 8.f) * kLn2 : -INFINITY;
+      for (int h = 0; h < 4; ++h) L[h] = aborted ? 0.f : redl[h] + redl[4 + h] + redl[8 + h] + redl[12 + h];
+      // ---- set 1 hands (m, L) over; set 0 merges and writes ---------------------------------------
+      float* mg = reinterpret_cast<float*>(smem + kOffMerge) + 8 * (k & 1);
+      const uint32_t mph = (k >> 1) & 1;
+      bool step_ok = !aborted;
+      // the item's last page of each set (page e0 + i with (e0 + i) % 2 == set)
+      const int el = e0 + n - 1, e_last = (el & 1) == set ? el : el - 1;
+      const bool has_pages = e_last >= e0;
+      if (set == 1) {
+        // this set's PVs are issued by their own thread, in order: once the last
+        // one is done, set 1's accumulator is final (every earlier PV of this
+        // set was seen complete by the P tile waits, so the parity wait sees its
+        // own phase); the hand-off below tells set 0
+        if (step_ok && has_pages)
+          step_ok = warp_wait(bar(kPVDone + e_last % kSlots), (e_last / kSlots) & 1, wc);
+        tc_fence_before();
+        if (step_ok) step_ok = warp_wait(bar(kMergeEmpty + (k & 1)), mph ^ 1, wc);
+        if (step_ok) {
+          if (row == 0) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              mg[h] = m_ref[h];
+              mg[4 + h] = L[h];
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kMergeFull + (k & 1)));
+        }
+      } else {
+        // both accumulators, once the item's last PV is done (thread = channel)
+        float o0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, o1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const bool has0 = has_pages, has1 = n > ((1 - e0) & 1);  // each set had a page of the item
+        // set 0's own accumulator once its last PV is done (its PVs come from one
+        // thread, in order); set 1's once set 1 has handed over, which it does
+        // only after its own last PV
+        if (step_ok && has0) step_ok = warp_wait(bar(kPVDone + e_last % kSlots), (e_last / kSlots) & 1, wc);
+        if (step_ok) step_ok = warp_wait(bar(kMergeFull + (k & 1)), mph, wc);
+        if (step_ok && n > 0) {
+          tc_fence_after();
+          if (has0) tmem_ld8(trow + kTmO + 16 * (2 * ob), o0);
+          if (has1) tmem_ld8(trow + kTmO + 16 * (2 * ob + 1), o1);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kOFree + ob));  // PVs of item ni + 2 may overwrite them
+        }
+        const size_t row0 = ((size_t)r->j * p.n_splits + r->split) * kQHeads + r->kvh * kGqa;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float m1 = step_ok ? mg[h] : -INFINITY, L1 = step_ok ? mg[4 + h] : 0.f;
+          const float m = fmaxf(m_ref[h], m1);
+          const float w0 = (m_ref[h] == -INFINITY || L[h] == 0.f) ? 0.f : fast_exp2(m_ref[h] - m);
+          const float w1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : fast_exp2(m1 - m);
+          const float Lm = L[h] * w0 + L1 * w1;
+          // a set without pages has weight 0 and an unread accumulator (stays 0)
+          const float om = (w0 > 0.f ? (o0[h] + o0[4 + h]) * w0 : 0.f) + (w1 > 0.f ? (o1[h] + o1[4 + h]) * w1 : 0.f);
+          const bool nonempty = step_ok && n > 0 && Lm > 0.f;
+          p.o_part[(row0 + h) * kHeadDim + row] = nonempty ? om / Lm * p.out_scale : 0.f;
+          if (row == 0) p.lse_part[row0 + h] = nonempty ? (m + log2f(Lm) - 8.f) * kLn2 : -INFINITY;
+        }
+        __syncwarp();
+        if (lane == 0 && step_ok) mbar_arrive(bar(kMergeEmpty + (k & 1)));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kRecEmpty + slot));
       if (n > 0) ++ni;
-      ok = !aborted;
+      e0 += n;
+      ok = step_ok;
     }
   }
 
@@ -608,7 +691,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
   if (tid == 0) {
     // every tcgen05.mma is done (both issuers committed after their last one)
     mbar_wait_drain(bar(kDone), 0, p.wait_ns);
-    mbar_wait_drain(bar(kDone + 1), 0, p.wait_ns);
     if (*s_abort) {
       set_status(p.status, MSA_STATUS_TIMEOUT);
       // bounded drain of the copies that may still be landing: the last
@@ -637,15 +719,14 @@ cudaError_t launch_sparse_attn_tc(const msa_cache* c, const uint8_t* q, float so
   static DeviceSetup setup;
   int dev = 0, n_sm = 0;
   cudaError_t e = setup.get(&dev, &n_sm, [](int) {
-    return cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)attn_smem_bytes(kMaxSeqs));
+    return cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptin);
   });
   if (e != cudaSuccess) return e;
   const int n_items = n_q_total * kKvHeads * n_splits;
   AttnParams ap{static_cast<const uint8_t*>(c->kv_pool), c->n_pages, q, sel, n_sel, block_table,
                 max_pages, seq_lens, q_start_loc, n_seqs, n_q_total, n_splits, n_items,
                 softmax_scale / c->s_enc_k * kLog2e, 1.0f / c->s_enc_v, o_part,
-                lse_part, c->status, launch_settings().wait_ns,
+                lse_part, c->status, launch_settings().wait_ns, qsl_fits(n_seqs) ? 1 : 0,
                 (launch_settings().inject & kInjectAttentionTimeout) ? 1 : 0};
   const int grid = n_items < n_sm ? n_items : n_sm;
   return launch_pdl(sparse_attn_tc_kernel, dim3(grid), dim3(kThreads), attn_smem_bytes(n_seqs), stream, ap);

@@ -296,6 +296,31 @@ def test_most_sequences_per_call():
     assert st.cache.read_status() == 0
 
 
+@pytest.mark.parametrize("n_seqs", [127, 128, 300])
+def test_sequence_lookup_with_empty_sequences(n_seqs):
+    # the attention finds each token's sequence by a search of q_start_loc,
+    # kept in shared memory for up to 127 sequences and read from global
+    # memory beyond; about 40% of the sequences here have no query token, so
+    # q_start_loc repeats values (a token belongs to the last sequence whose
+    # start is <= it)
+    rng = np.random.default_rng(1000 + n_seqs)
+    lens = [int(x) for x in rng.integers(1, 3000, n_seqs)]
+    n_q = [0 if rng.random() < 0.4 else int(rng.integers(1, 5)) for _ in range(n_seqs)]
+    n_q = [min(a, L) for a, L in zip(n_q, lens)]
+    n_q[-1] = 0  # an empty sequence at the end as well
+    wl = workloads.custom("lookup_%d" % n_seqs, lens, n_q, seed=n_seqs, permuted=True)
+    st = harness.build_state(wl, DEV)
+    side = OracleSide(wl, DEV)
+    bufs, out, S = _decode(wl, st)
+    T = wl.n_q_total
+    starts = np.asarray(wl.q_start_loc)
+    # the first token after each run of empty sequences, and a few at random
+    after_empty = [int(starts[b]) for b in range(1, n_seqs) if n_q[b - 1] == 0 and n_q[b] > 0]
+    tokens = sorted(set([0, T - 1] + after_empty[:6] + [int(x) for x in rng.integers(0, T, 4)]))
+    _check_tokens(wl, side, bufs, out, S, tokens)
+    assert st.cache.read_status() == 0
+
+
 def test_host_validation_errors(tiny):
     wl, st, _ = tiny
     q, qi, w = wl.queries(DEV)
