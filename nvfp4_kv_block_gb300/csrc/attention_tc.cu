@@ -15,9 +15,10 @@
 // wait bounded:
 //   warp 0       scheduler and TMA producer: per item, the sequence of j
 //                (a 32-way search of q_start_loc, copied to shared memory when
-//                it fits beside the rings), the selected blocks, their
-//                physical pages and the tokens visible in each, and the 4 query
-//                rows as a swizzled tile, into a ring of kRecs item records;
+//                it fits beside the rings: up to 115 sequences), the selected
+//                blocks, their physical pages and the tokens visible in each,
+//                and the 4 query rows as a swizzled tile, into a ring of kRecs
+//                item records;
 //                then one 18,432-byte cp.async.bulk copy per page of the item
 //                (the KV head's K and V codes and scales) into a ring of stages;
 //   warps 1-2    QK issuers, warp 1 + s for the pages of set s (e % 2 == s):
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(AttnParams 
       if (ok && lane == 0) mbar_arrive(bar(kRecEmpty + slot));
     }
   } else if (warp >= kWarpSmax0) {
-    // ---------------- softmax: set s = warps 4 + 4 s .. 7 + 4 s --------------------------------
+    // ---------------- softmax: set s = warps 5 + 4 s .. 8 + 4 s --------------------------------
     // set s takes the pages with e % 2 == s (S slot s); warp w reads TMEM lanes
     // 32 (w % 4) ..: row = token of S, channel of O
     const int set = (warp - kWarpSmax0) >> 2, quad = warp & 3, row = 32 * quad + lane;
