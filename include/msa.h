@@ -36,9 +36,12 @@
  * Page formats (one physical page id p addresses both pools):
  *   KV page p at kv_pool + p * 73,728 bytes = 4 heads x 18,432 bytes; head g
  *   at offset g * 18,432:
- *     +0       K codes  [128 tokens][64 B]: byte i = code(ch 2i) | code(ch 2i+1) << 4,
- *              with the 16-byte chunk c (channels 32c..32c+31) of token t stored
- *              at chunk position c XOR ((t >> 1) mod 4) of its row
+ *     +0       K codes  [128 tokens][64 B]: little-endian 32-bit word i of a
+ *              row holds channels 8i..8i+7 as E2M1 codes (sign s, magnitude m):
+ *              m of channel 8i+n at bits 4n..4n+2 (n = 0..7), s of channel 8i+n
+ *              at bit 8n+7 and s of channel 8i+4+n at bit 8n+3 (n = 0..3); the
+ *              16-byte chunk c (channels 32c..32c+31) of token t is stored at
+ *              chunk position c XOR ((t >> 1) mod 4) of its row
  *     +8,192   K scales [8 groups][128 tokens]: E4M3 scale of channels 16k..16k+15
  *     +9,216   V codes  [128 tokens][64 B], chunks placed like the K codes
  *     +17,408  V scales [8 groups][128 tokens]

@@ -179,21 +179,33 @@ __device__ __forceinline__ void build_dequant_table(uint2* tab, int tid, int nth
   }
 }
 
-// Eight E2M1 codes (nibble k = element k) -> eight FP8 operand bytes
-// (x: elements 0..3, y: elements 4..7), each sign(code) | table[|code|].
-// Magnitudes: byte permutes of the scaled table by the 3-bit codes.  Signs:
-// element k's sign is bit 3 of nibble k; for even k that is bit 7 of byte k/2
-// of (w << 4), for odd k bit 7 of byte k/2 of w, so one more byte permute per
-// four elements places every sign bit at bit 7 of its output byte.  9 integer
-// instructions per 8 elements.
+// Code word: little-endian 32-bit word i of a token's code row holds channels
+// 8i..8i+7, each an E2M1 code (sign << 3 | 3-bit magnitude): the magnitude of
+// channel n at bits 4n..4n+2 (n = 0..7), the sign of channel n at bit 8n+7 and
+// that of channel 4 + n at bit 8n+3 (n = 0..3).  The magnitudes are then the
+// byte-permute selectors of dequant8 as they stand, and each sign bit sits at,
+// or 4 bits below, bit 7 of its output byte.
+// Bits of channels 4h..4h+3 (h = 0 or 1) of a word, codes c[0..3].
+__host__ __device__ __forceinline__ uint32_t code_word_part(const uint32_t (&c)[4], int h) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    w |= (c[n] & 7u) << (16 * h + 4 * n);
+    w |= ((c[n] >> 3) & 1u) << (8 * n + (h ? 3 : 7));
+  }
+  return w;
+}
+
+// One code word -> eight FP8 operand bytes (x: channels 0..3, y: 4..7), each
+// sign(code) | table[magnitude]: two byte permutes of the scaled table by the
+// magnitudes (sign bits masked out: a set selector bit 3 would switch the
+// permute to sign replication), the sign bits merged in place (x) or after a
+// 4-bit shift (y).  7 integer instructions per 8 elements.
 __device__ __forceinline__ uint2 dequant8(uint32_t w, uint2 t) {
   const uint32_t m = w & 0x77777777u;
   const uint32_t mag0 = prmt(t.x, t.y, m);
   const uint32_t mag1 = prmt(t.x, t.y, m >> 16);
-  const uint32_t w4 = w << 4;
-  const uint32_t s0 = prmt(w4, w, 0x5140u);  // bytes: w4.b0, w.b0, w4.b1, w.b1
-  const uint32_t s1 = prmt(w4, w, 0x7362u);  // bytes: w4.b2, w.b2, w4.b3, w.b3
-  return make_uint2(mag0 | (s0 & 0x80808080u), mag1 | (s1 & 0x80808080u));
+  return make_uint2(mag0 | (w & 0x80808080u), mag1 | ((w << 4) & 0x80808080u));
 }
 
 // ---- mbarrier / TMA bulk copy / tcgen05 (inline PTX) --------------------------

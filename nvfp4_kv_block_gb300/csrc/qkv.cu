@@ -114,11 +114,15 @@ __device__ __forceinline__ void store_nvfp4_row(const float (&y)[128], float s_e
     for (int w2 = 0; w2 < 2; ++w2) {
       uint32_t word = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float v = y[16 * gq + 8 * w2 + i];
-        uint32_t c = e2m1_code(__fmul_rn(fabsf(v), s_enc), sb);
-        c |= (v < 0.f && c) ? 8u : 0u;
-        word |= c << (4 * i);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float v = y[16 * gq + 8 * w2 + 4 * h + i];
+          c[i] = e2m1_code(__fmul_rn(fabsf(v), s_enc), sb);
+          c[i] |= (v < 0.f && c[i]) ? 8u : 0u;
+        }
+        word |= code_word_part(c, h);
       }
       words[2 * gq + w2] = word;
     }

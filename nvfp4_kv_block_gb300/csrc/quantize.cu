@@ -71,13 +71,17 @@ __global__ void __launch_bounds__(256) quantize_insert_kernel(
     c1 |= (x.y < 0.f && c1) ? 8u : 0u;
     c2 |= (x.z < 0.f && c2) ? 8u : 0u;
     c3 |= (x.w < 0.f && c3) ? 8u : 0u;
-    const uint16_t packed = (uint16_t)(c0 | (c1 << 4) | (c2 << 8) | (c3 << 12));
+    // lanes 2i and 2i + 1 make code word i (channels 8i..8i+7) together
+    const uint32_t cs[4] = {c0, c1, c2, c3};
+    const uint32_t part = code_word_part(cs, lane & 1);
+    const uint32_t word = part | __shfl_xor_sync(0xffffffffu, part, 1);
     uint8_t* head = kv_pool + (size_t)page * kKvPageBytes + g * kHeadBytes;
     const int off_c = is_v ? kOffVc : kOffKc;
     const int off_s = is_v ? kOffVs : kOffKs;
-    // lane l's two bytes: offset 2l & 15 of code chunk l >> 3
-    *reinterpret_cast<uint16_t*>(head + off_c + off * 64 + (code_chunk_pos(lane >> 3, off) << 4) +
-                                 ((lane & 7) << 1)) = packed;
+    // word i = lane >> 1: offset 4 (i & 3) of code chunk i >> 2
+    if ((lane & 1) == 0)
+      *reinterpret_cast<uint32_t*>(head + off_c + off * 64 + (code_chunk_pos(lane >> 3, off) << 4) +
+                                   (((lane >> 1) & 3) << 2)) = word;
     if ((lane & 3) == 0) head[off_s + (lane >> 2) * kPageTokens + off] = (uint8_t)sb_byte;
   }
 }

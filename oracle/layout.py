@@ -10,9 +10,12 @@ placement of bytes inside a page is this library's own format, restated here
 independently of the CUDA code from its written specification:
 
 KV page, 73,728 bytes = 4 heads x 18,432 bytes; head g starts at g * 18,432:
-    +0      K codes   [128 tokens][64 B]  byte i = code(2i) | code(2i+1) << 4,
-            except that the 16-byte chunk c of token t's row (channels
-            32c..32c+31) is stored at chunk position c XOR ((t >> 1) mod 4)
+    +0      K codes   [128 tokens][64 B]: little-endian 32-bit word i holds
+            channels 8i..8i+7 (E2M1 code = sign bit s and magnitude m, 3 bits):
+            bits 4n..4n+2 = m of channel 8i+n (n = 0..7), bit 8n+7 = s of
+            channel 8i+n and bit 8n+3 = s of channel 8i+4+n (n = 0..3); the
+            16-byte chunk c of token t's row (channels 32c..32c+31) is stored
+            at chunk position c XOR ((t >> 1) mod 4)
     +8,192  K scales  [8 groups][128 tokens]   E4M3, group k = channels 16k..16k+15
     +9,216  V codes   [128 tokens][64 B], chunks placed like the K codes
     +17,408 V scales  [8 groups][128 tokens]
@@ -38,17 +41,35 @@ OFF_KC, OFF_KS, OFF_VC, OFF_VS = 0, 8_192, 9_216, 17_408
 
 
 def pack_codes(codes):
-    """Pack E2M1 codes (last axis even) two per byte, element 2i in the low nibble."""
-    c = np.asarray(codes, dtype=np.uint8)
-    return (c[..., 0::2] & 15) | ((c[..., 1::2] & 15) << 4)
+    """Pack E2M1 codes (4-bit: sign << 3 | magnitude; last axis a multiple of 8)
+    into 32-bit little-endian words of 8 channels each, as laid out above."""
+    c = np.asarray(codes, dtype=np.uint32)
+    g = c.reshape(c.shape[:-1] + (c.shape[-1] // 8, 8))
+    mag, sign = g & 7, (g >> 3) & 1
+    word = np.zeros(g.shape[:-1], dtype=np.uint32)
+    for n in range(8):
+        word |= mag[..., n] << (4 * n)
+    for n in range(4):
+        word |= sign[..., n] << (8 * n + 7)
+        word |= sign[..., 4 + n] << (8 * n + 3)
+    out = np.empty(word.shape + (4,), dtype=np.uint8)
+    for b in range(4):
+        out[..., b] = (word >> (8 * b)) & 0xFF
+    return out.reshape(c.shape[:-1] + (c.shape[-1] // 2,))
 
 
 def unpack_codes(packed):
-    p = np.asarray(packed, dtype=np.uint8)
-    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
-    out[..., 0::2] = p & 15
-    out[..., 1::2] = p >> 4
-    return out
+    """Inverse of pack_codes."""
+    p = np.asarray(packed, dtype=np.uint32)
+    b = p.reshape(p.shape[:-1] + (p.shape[-1] // 4, 4))
+    word = b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16) | (b[..., 3] << 24)
+    out = np.empty(word.shape + (8,), dtype=np.uint8)
+    for n in range(8):
+        out[..., n] = (word >> (4 * n)) & 7
+    for n in range(4):
+        out[..., n] |= (((word >> (8 * n + 7)) & 1) << 3).astype(np.uint8)
+        out[..., 4 + n] |= (((word >> (8 * n + 3)) & 1) << 3).astype(np.uint8)
+    return out.reshape(p.shape[:-1] + (p.shape[-1] * 2,))
 
 
 def code_chunk_position(c, t):

@@ -138,7 +138,7 @@ def test_layout_hand_offsets():
     key = np.arange(128, dtype=np.uint8)
     with open(os.path.join(GOLDEN, "layout_bytes.txt")) as f:
         rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
-    for what, head, tok, el, off in rows:
+    for what, head, tok, el, off, *bits in rows:
         tok, el, off = int(tok), int(el), int(off)
         pool[:] = 0
         ipool[:] = 0
@@ -150,8 +150,9 @@ def test_layout_hand_offsets():
         g = int(head)
         if what in ("kcode", "vcode"):
             c = kc if what == "kcode" else vc
-            nib = pool[0, off] >> 4 if el % 2 else pool[0, off] & 15
-            assert nib == c[g, el]
+            shift, sign_off, sign_bit = (int(x) for x in bits)
+            assert (pool[0, off] >> shift) & 7 == c[g, el] & 7
+            assert (pool[0, sign_off] >> sign_bit) & 1 == c[g, el] >> 3
         else:
             s = ks if what == "kscale" else vs
             assert pool[0, off] == s[g, el]
