@@ -256,6 +256,22 @@ def test_topk_of_long_rows_matches_oracle(ctx):
     assert st.cache.read_status() == 0
 
 
+
+@pytest.mark.parametrize("ctx", [4800 * 128 + 1, 9000 * 128 + 1])
+def test_topk_of_long_rows_several_tokens_per_cta(ctx):
+    # More query tokens than CTAs (a CTA selects for several tokens in turn,
+    # reusing its buffers) with long rows: ~4,800 blocks (keys held in
+    # registers) and ~9,000 (staged in shared memory).  Tokens j and
+    # j + (number of SMs) share a CTA.
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = workloads.custom(f"pairs_{ctx}", [ctx], [n_sm + 8], seed=93)
+    st = harness.build_state(wl, DEV)
+    side = OracleSide(wl, DEV)
+    bufs, out, S = _decode(wl, st)
+    _check_tokens(wl, side, bufs, out, S, [0, 1, n_sm, n_sm + 1, n_sm + 7])
+    assert np.isfinite(out).all()
+    assert st.cache.read_status() == 0
+
 def test_hand_computed_indexer_case_on_the_gpu():
     # The hand-computed case of tests/golden/indexer_tiny.txt through the
     # library: insert its index keys, scan, select.
@@ -320,6 +336,37 @@ def test_sequence_lookup_with_empty_sequences(n_seqs):
     _check_tokens(wl, side, bufs, out, S, tokens)
     assert st.cache.read_status() == 0
 
+
+
+def test_inconsistent_q_start_loc_is_flagged_without_a_wait():
+    # with a q_start_loc that leaves a token outside every sequence, or makes
+    # two sequences overlap, every token still gets an output (an empty
+    # selection where it has no sequence), the status says BAD_SEQ, and no
+    # wait runs out
+    wl = workloads.custom("qsl_bad", [3000, 5000], [2, 2], seed=21)
+    st = harness.build_state(wl, DEV)
+    _, qi, w = wl.queries(DEV)
+    ref_sel, ref_n, _ = ops.indexer_topk(st.cache, qi, w, st.block_table, st.seq_lens, st.q_start_loc)
+    torch.cuda.synchronize()
+    ref_sel, ref_n = ref_sel.cpu().numpy(), ref_n.cpu().numpy()
+    assert st.cache.read_status() == 0
+    # token 3 outside every sequence (q_start_loc ends at 3 of 4 tokens)
+    qsl = torch.tensor([0, 2, 3], dtype=torch.int32, device=DEV)
+    sel, n_sel, _ = ops.indexer_topk(st.cache, qi, w, st.block_table, st.seq_lens, qsl)
+    torch.cuda.synchronize()
+    sel, n_sel = sel.cpu().numpy(), n_sel.cpu().numpy()
+    assert st.cache.read_status() & ops.STATUS_BAD_SEQ
+    assert not st.cache.read_status() & ops.STATUS_TIMEOUT
+    assert n_sel[3] == 0 and (sel[3] == -1).all()
+    assert np.array_equal(sel[:2], ref_sel[:2]) and np.array_equal(n_sel[:2], ref_n[:2])
+    # overlapping sequences (q_start_loc not non-decreasing)
+    st.cache.status.zero_()
+    qsl = torch.tensor([0, 3, 2], dtype=torch.int32, device=DEV)
+    sel, n_sel, _ = ops.indexer_topk(st.cache, qi, w, st.block_table, st.seq_lens, qsl)
+    torch.cuda.synchronize()
+    assert st.cache.read_status() & ops.STATUS_BAD_SEQ
+    assert not st.cache.read_status() & ops.STATUS_TIMEOUT
+    assert (n_sel.cpu().numpy() >= 0).all()
 
 def test_host_validation_errors(tiny):
     wl, st, _ = tiny
