@@ -61,6 +61,9 @@ constexpr int kSlots = 6;      // K8 buffers (tensor memory), V8 tiles and P til
 // never to see a phase two behind, the same group must own every page of a
 // slot (and of a stage): kGroups divides both ring sizes.
 static_assert(kSlots % kGroups == 0 && kStages % kGroups == 0, "groups own whole slots and stages");
+// Likewise a softmax set reuses the P tile (and waits on the PV commit) of its
+// own page e - kSlots: kSets divides kSlots.
+static_assert(kSlots % kSets == 0, "sets own whole P tiles");
 constexpr int kTileBytes = 16384;                      // [128 rows][128 B], swizzled
 constexpr int kOffV8 = 0;                              // kSlots V8 tiles
 constexpr int kOffQ = kSlots * kTileBytes;             // kRecs x [16 rows][128 B]
