@@ -506,7 +506,7 @@ def main():
         dev = "cuda" if torch.cuda.is_available() else "cpu"
         qps, cores, sample = oracle_sample(wl, dev, args.cpu_budget)
         line = {"impl": "reference", "metric": "decode query tokens/s (NVFP4 sparse attention)",
-                "value": qps, "unit": "queries/s", "n_gpus": 0, "steps": args.steps,
+                "value": qps, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": qps, "unit": "queries/s", "cores": cores, "kind": "oracle",
